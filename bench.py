@@ -1,0 +1,338 @@
+"""Throughput of the SCAPE optimizer step on one GB300 (or N independent replicas).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl scape|reference]
+                    [--workload NAME] [--density D]
+
+A step is one pass of the whole hot path (offsets of M_{t-1}, the per-worker
+streaming pass, the fixed-order reduction with the AdamS update, the
+partitioned top-k) over one batch of W synthetic bf16 gradients already
+resident in HBM.  Default workload: the Llama-style 1775.4M-parameter layout,
+W=4 emulated workers, density 0.01, chunk 65536.  Prints one JSON line.
+
+--impl reference times the CPU oracle instead (single thread, host cores) on a
+bounded sample of whole chunks of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "SCAPE optimizer step params/s and achieved HBM GB/s (% of 8 TB/s) on 1 GB300"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="scape", choices=["scape", "reference"])
+    ap.add_argument("--workload", default=synth.BENCH_WORKLOAD, choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--density", type=float, default=None)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def alg_bytes(N: int, W: int, K: int) -> dict:
+    """Algorithmic (compulsory) HBM bytes per step and per kernel.
+    stream_compact: W*N*(2 g + 8 u + 8 e + 1/8 mask) + W*K*4 (kept values written)
+    reduce_update:  N*(8 theta + 8 v + 1/8 mask) + K*(4W vals read + 4 bbar + 4 idx)
+    select:         N*(1/8 new mask)  (+4 B/param re-read of a, not counted)
+    """
+    a = W * N * (2 + 8 + 8 + 0.125) + W * K * 4
+    b = N * (8 + 8 + 0.125) + K * (4 * W + 8)
+    c = N * 0.125
+    return {"stream_compact": a, "reduce_update": b, "select": c, "step": a + b + c}
+
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.p = None
+        self.idx = gpu_index
+
+    def start(self):
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}",
+                                       "--format=csv,noheader,nounits", "-i", str(self.idx),
+                                       "-lms", "100"], stdout=subprocess.PIPE,
+                                      stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.p = None
+
+    def stop(self) -> dict | None:
+        if self.p is None:
+            return None
+        self.p.terminate()
+        try:
+            out, _ = self.p.communicate(timeout=5)
+        except Exception:
+            self.p.kill()
+            out, _ = self.p.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 7:
+                continue
+            try:
+                sm.append(float(f[0]))
+                smax.append(float(f[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def ncu_traffic(kernel: str, workload: str):
+    """Per-launch DRAM bytes from the committed ncu summary, if it was taken on
+    the current source of the kernel (else None)."""
+    src = {"stream_compact": "k_stream.cu"}.get(kernel)
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    if not src or not os.path.exists(path):
+        return None
+    h = hashlib.sha256(open(os.path.join(ROOT, "sparse_communication_distributed_gb300", "csrc",
+                                         src), "rb").read()).hexdigest()[:16]
+    for line in open(path):
+        f = line.split()
+        if len(f) >= 4 and f[0] == kernel and f[1] == workload and f[3] == h:
+            return float(f[2])
+    return None
+
+
+def oracle_sample(wl, density, n_chunks: int, steps: int):
+    """Time the oracle (as it stands) on n_chunks whole chunks spread over the
+    shards; returns (params/s, seconds, sample params)."""
+    import oracle
+    nch = -(-wl.N // wl.chunk)
+    ids = np.unique(np.linspace(0, nch - 1, n_chunks).astype(np.int64))
+    o = oracle.Oracle.for_workload(wl, density, chunk_ids=ids)
+    o.set(oracle.THETA, synth.cpu().theta0(wl, o.index))
+    grads = [np.stack([synth.cpu().grads(wl, w, t, idx=o.index) for w in range(wl.W)])
+             for t in range(steps)]
+    t0 = time.perf_counter()
+    for t in range(steps):
+        o.step(grads[t])
+    dt = time.perf_counter() - t0
+    return o.n * steps / dt, dt, o.n, ids.size
+
+
+def run_reference(args, wl, density):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    n_chunks = 16 if wl.N > 1 << 24 else max(1, min(16, -(-wl.N // wl.chunk)))
+    steps = args.warmup + args.steps
+    rate, dt, n, nc = oracle_sample(wl, density, n_chunks, steps)
+    per_step_ms = dt / steps * 1e3
+    sample = (f"{nc} whole chunks ({n} params) of {wl.name}, W={wl.W}, density {density}, "
+              f"{steps} steps incl. step 0; single-threaded C++ oracle")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": rate, "unit": "params/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": per_step_ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": wl.name, "N": wl.N, "W": wl.W, "density": density,
+                   "chunk": wl.chunk, "sample_params": n},
+        "cpu_baseline": {"value": rate, "unit": "params/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": rate, "unit": "params/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_scape(args, wl, density):
+    import torch
+    from sparse_communication_distributed_gb300 import THETA, Scape
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+
+    def barrier():
+        if pg:
+            pg.barrier()
+
+    N, W = wl.N, wl.W
+    sc = Scape.for_workload(wl, density)
+    K = sc.K
+    th = torch.empty(N, dtype=torch.float32, device=dev)
+    synth.gpu().theta_into(wl, th)
+    torch.cuda.synchronize()
+    sc.load(THETA, th)
+    del th
+    n_batches = 2
+    batches = []
+    for b in range(n_batches):
+        bufs = [torch.empty(N, dtype=torch.int16, device=dev) for _ in range(W)]
+        for w in range(W):
+            synth.gpu().grads_into(wl, w, b, bufs[w])
+        batches.append(bufs)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream(dev)
+
+    for i in range(args.warmup):
+        sc.step(batches[i % n_batches], stream)
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    for i in range(args.steps):
+        sc.step(batches[i % n_batches], stream)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    ms = ev0.elapsed_time(ev1)
+    # per-kernel breakdown: the same steps again with events around each phase
+    sc.profile(True)
+    for i in range(args.steps):
+        sc.step(batches[i % n_batches], stream)
+    torch.cuda.synchronize()
+    phases = sc.profile_read()
+    sc.profile(False)
+    clk = clocks.stop()
+
+    ms_max = ms
+    if pg:
+        t = torch.tensor([ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms_max = float(t.item())
+    ms_per_step = ms_max / args.steps
+
+    # end to end through the public API: host gradients in, mask out
+    e2e = None
+    if not args.no_e2e:
+        host = [batches[0][w].cpu().pin_memory() for w in range(W)]
+        out = torch.empty(sc.info["mask_words"], dtype=torch.int32).pin_memory()
+        e2e_steps = min(args.steps, 5)
+        sc.step_host(host, stream)
+        sc.mask_into(out)
+        barrier()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(e2e_steps):
+            sc.step_host(host, stream)
+            sc.mask_into(out)
+        torch.cuda.synchronize()
+        dt = time.perf_counter() - t0
+        if pg:
+            t = torch.tensor([dt], device=dev)
+            pg.all_reduce(t, op=pg.ReduceOp.MAX)
+            dt = float(t.item())
+        e2e = {"value": world * N * e2e_steps / dt, "unit": "params/s",
+               "h2d_bytes_per_step": W * N * 2, "d2h_bytes_per_step": sc.info["mask_words"] * 4,
+               "ms_per_step": dt / e2e_steps * 1e3, "steps": e2e_steps}
+        del host, out
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, dt, n, nc = oracle_sample(wl, density, 64 if N > 1 << 24 else 16, 4)
+        cpu = {"value": rate, "unit": "params/s", "cores": 1, "kind": "oracle",
+               "sample": f"{nc} whole chunks ({n} params) of {wl.name}, W={W}, density {density}, "
+                         f"4 steps incl. step 0, {dt:.1f} s; single-threaded C++ oracle"}
+
+    if rank != 0:
+        return
+    peak, peak_kind = measured_peak()
+    ab = alg_bytes(N, W, K)
+    a_ms, a_n = phases["stream_compact"]
+    a_launch_ms = a_ms / max(a_n, 1)
+    achieved = ab["stream_compact"] / (a_launch_ms * 1e-3) / 1e9
+    step_gbs = ab["step"] / (ms_per_step * 1e-3) / 1e9
+    line = {
+        "metric": METRIC,
+        "value": world * N / (ms_per_step * 1e-3),
+        "unit": "params/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_per_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": wl.name, "N": N, "W": W, "density": density, "chunk": wl.chunk,
+                   "K": K, "grad_dtype": "bf16", "grad_batches": n_batches,
+                   "parallelism": "replicas" if world > 1 else "single GPU, W emulated workers",
+                   "l2": f"no flush: {sc.info['device_bytes'] / 1e9:.1f} GB resident state, "
+                         "far larger than L2"},
+        "step_hbm": {"alg_bytes_per_step": ab["step"], "achieved_gbs": step_gbs,
+                     "frac_of_8tbs": step_gbs / NOMINAL_HBM_GBS,
+                     "frac_of_peak": step_gbs / peak, "peak_kind": peak_kind},
+        "roofline": {"kernel": "stream_compact", "bound": "hbm", "achieved": achieved,
+                     "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": ncu_traffic("stream_compact", wl.name),
+                     "alg_bytes_per_launch": ab["stream_compact"], "launch_ms": a_launch_ms,
+                     "peak_kind": f"{peak_kind} (hbm_gbs)"},
+        "kernels_ms_per_step": {k: v[0] / args.steps for k, v in phases.items() if v[1]},
+        "gpu_launches": args.steps * 5,
+        "clocks": clk,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    if pg:
+        pg.destroy_process_group()
+
+
+def main():
+    args = parse()
+    wl = synth.WORKLOADS[args.workload]
+    density = args.density if args.density is not None else wl.densities[0]
+    if args.impl == "reference":
+        run_reference(args, wl, density)
+    else:
+        run_scape(args, wl, density)
+
+
+if __name__ == "__main__":
+    main()

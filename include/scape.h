@@ -1,0 +1,169 @@
+/*
+ * libscape — the SCAPE sparse-communication optimizer step on one GPU
+ * (sm_103a), as a C ABI.
+ *
+ * Method: "SCAPE: Accurate and Efficient LLM Training with Extreme Sparse
+ * Communication" (arXiv 2607.01678) — abstract; gist.science technical
+ * summary §2 "Methodology" (AdamS base optimizer; partitioned mask
+ * synchronization; delayed mask usage; single-buffer second-moment
+ * reconstruction; packed single-bit masks).  W data-parallel workers are
+ * emulated as W gradient replicas in one GPU's memory; the all-reduce of the
+ * sparse buffer becomes a fixed-order sum and the all-gather of the shard
+ * masks becomes their concatenation in one bitmap.
+ *
+ * One step t, per coordinate i and worker w (fp32, no fused multiply-add):
+ *   u_w   = b1*u_w + (1-b1)*g_w
+ *   a_w   = e_w + u_w
+ *   b_w   = M_{t-1}[i] ? a_w : +0          (mask built at step t-1)
+ *   e_w   = a_w - b_w
+ *   bbar  = (b_0 + b_1 + ... + b_{W-1}) * (1/W)   (left to right)
+ *   v     = b2*v + (1-b2)*(bbar*bbar)
+ *   theta = theta - lr*(bbar/(sqrt(v)+eps) + wd*theta)
+ * then M_t: the flat vector is cut into chunks of C coordinates; worker w owns
+ * chunks [w*q, (w+1)*q), q = ceil(n_chunks/W), and in each of them keeps the
+ * k_c = floor(density*len_c) coordinates of largest |a_w| (as fp32 bits with
+ * the sign cleared), equal keys going to the lower index.  Every chunk thus
+ * carries exactly k_c coordinates and K = sum_c k_c values are exchanged per
+ * worker per step.  At step 0, M_{-1} is this selection applied to the step-0
+ * accumulators (before anything is written).
+ *
+ * Conventions for every entry point:
+ *   - Return value: SCAPE_OK (0) or a negative SCAPE_E* code; the handle's
+ *     message (scape_last_error) says what failed.  Argument errors are found
+ *     before anything is enqueued; SCAPE_ECUDA reports a CUDA runtime error.
+ *   - "stream" is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  scape_step* only enqueue work on it and return; readers
+ *     (scape_mask, scape_read_*) first wait for the last step's stream.
+ *   - Pointers documented as "host or device" may be either (copies use
+ *     cudaMemcpyDefault under unified addressing).
+ *   - A handle is not thread-safe; separate handles are independent.
+ *   - Limits: 1 <= W <= 64; 0 < density <= 1; chunk a multiple of 32 in
+ *     [32, 65536]; 0 < N < 2^32.
+ */
+#ifndef SCAPE_H
+#define SCAPE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct scape_handle scape_handle; /* opaque, owned by the library */
+
+/* Flat parameter layout: the concatenation of n_tensors tensors of numel[]
+ * coordinates (N = sum numel).  Chunks tile the flat vector and ignore tensor
+ * boundaries. numel is read during scape_create only. */
+typedef struct {
+  uint32_t n_tensors;
+  const uint64_t* numel;
+  uint32_t chunk;
+} scape_layout;
+
+enum {
+  SCAPE_OK = 0,
+  SCAPE_EINVAL = -1, /* bad argument */
+  SCAPE_ENOMEM = -2, /* device or host allocation failed */
+  SCAPE_ECUDA = -3,  /* CUDA runtime error (message has the CUDA error string) */
+  SCAPE_ESTATE = -4  /* call not valid in the handle's state (e.g. no mask yet) */
+};
+
+/* State fields for scape_read_state / scape_load_state. Element types:
+ * THETA, V, U, E: fp32; MASK: uint32 words (bit j of word i = coordinate
+ * 32i+j); STEP: one int64 (the step counter t). */
+enum { SCAPE_THETA = 0, SCAPE_V = 1, SCAPE_U = 2, SCAPE_E = 3, SCAPE_MASK = 4, SCAPE_STEP = 5 };
+
+/* Kernel phases reported by scape_profile_read. */
+enum {
+  SCAPE_PH_SELECT_BOOT = 0, /* step 0 only: M_{-1} from the step-0 accumulators */
+  SCAPE_PH_OFFSETS = 1,     /* prefix counts of M_{t-1} (compaction offsets) */
+  SCAPE_PH_STREAM = 2,      /* momentum, accumulate, mask-apply, residual, compaction */
+  SCAPE_PH_UPDATE = 3,      /* fixed-order W-way sum, second moment, AdamS update */
+  SCAPE_PH_SELECT = 4,      /* partitioned per-chunk top-k -> M_t */
+  SCAPE_PH_H2D = 5,         /* scape_step_host: host -> device gradient copies */
+  SCAPE_N_PHASES = 6
+};
+
+typedef struct {
+  uint64_t N;          /* coordinates */
+  uint32_t W;          /* emulated workers */
+  uint32_t chunk;      /* C */
+  uint64_t n_chunks;   /* ceil(N / C) */
+  uint64_t chunks_per_worker; /* q */
+  uint32_t k_full;     /* k of a full chunk */
+  uint32_t k_last;     /* k of the last chunk */
+  uint64_t K;          /* values per worker per step */
+  uint64_t mask_words; /* ceil(N / 32) */
+  int64_t step;        /* steps taken (t) */
+  uint64_t device_bytes; /* device memory held by the handle */
+} scape_info_t;
+
+/* Create a handle: computes the chunk/shard table, allocates all state on the
+ * current CUDA device (theta, v: N fp32; u, e: W x N fp32; two N-bit masks;
+ * K-entry compact buffers) and zeroes it.  Set theta with scape_load_state.
+ * On failure *out is NULL and nothing is leaked. */
+int scape_create(const scape_layout* layout, int W, double density, float beta1, float beta2,
+                 float lr, float wd, float eps, scape_handle** out);
+
+/* One optimizer step.  grad_ptrs: HOST array of W DEVICE pointers, each to N
+ * bf16 gradients (16-byte aligned), borrowed read-only until the step has
+ * completed on "stream".  Enqueues the step's kernels and returns. */
+int scape_step(scape_handle* h, const void* const* grad_ptrs, void* stream);
+
+/* The same step from HOST gradients: W host pointers to N bf16 each (pinned
+ * memory gives full copy speed).  The first call allocates a W x N bf16
+ * device staging buffer owned by the handle; each call enqueues the W
+ * host-to-device copies and the step on "stream" and returns. */
+int scape_step_host(scape_handle* h, const void* const* host_grad_ptrs, void* stream);
+
+/* Copy M_t, the mask built by the last step (applied at the next one), into
+ * out_bits (mask_words uint32, host or device).  Waits for the last step.
+ * SCAPE_ESTATE before the first step (unless a mask was loaded). */
+int scape_mask(scape_handle* h, uint32_t* out_bits);
+
+/* Free everything the handle owns (waits for its last step). NULL is a no-op. */
+void scape_destroy(scape_handle* h);
+
+/* Sizes and counters of the handle. */
+int scape_info(const scape_handle* h, scape_info_t* out);
+
+/* Copy elements [offset, offset+count) of a state field (worker w for U and
+ * E; ignored otherwise) to dst (host or device).  MASK counts words and gives
+ * M_t; STEP copies one int64 (offset 0, count 1).  Waits for the last step. */
+int scape_read_state(scape_handle* h, int which, int w, void* dst, uint64_t offset,
+                     uint64_t count);
+
+/* Overwrite elements [offset, offset+count) of a state field from src (host
+ * or device).  A MASK load must cover all words and carry exactly k_c bits in
+ * every chunk (checked; SCAPE_EINVAL otherwise); it becomes the mask the next
+ * step applies, so that step does no step-0 selection.  STEP sets t. */
+int scape_load_state(scape_handle* h, int which, int w, const void* src, uint64_t offset,
+                     uint64_t count);
+
+/* The last step's compact buffers, in ascending coordinate order: w in [0,W)
+ * gives worker w's kept values b_w, w = -1 the synchronized buffer bbar.
+ * Copies entries [offset, offset+count) to idx (uint32 coordinates, may be
+ * NULL) and vals (fp32, may be NULL), host or device; *total (may be NULL)
+ * receives K.  SCAPE_ESTATE before the first step. */
+int scape_read_sparse(scape_handle* h, int w, uint32_t* idx, float* vals, uint64_t offset,
+                      uint64_t count, uint64_t* total);
+
+/* Message of the handle's last error ("" if none).  Valid until the next call
+ * on the handle.  h == NULL gives the message of the last failed
+ * scape_create on this thread. */
+const char* scape_last_error(const scape_handle* h);
+
+/* enable != 0: every later step records CUDA events around each kernel phase
+ * on its stream (no extra synchronisation). enable == 0 stops recording. */
+int scape_profile(scape_handle* h, int enable);
+
+/* Sum of the recorded phase durations in ms (ms[SCAPE_N_PHASES]) and the
+ * number of recorded launches of each (launches[SCAPE_N_PHASES]); waits for
+ * the recorded events, then clears the record. */
+int scape_profile_read(scape_handle* h, double* ms, uint32_t* launches);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif

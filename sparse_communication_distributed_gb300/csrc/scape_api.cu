@@ -1,0 +1,537 @@
+// Host side of libscape: argument checks, the chunk/shard table, device
+// allocation, the launch sequence of one step and state read-back.  The
+// operations are documented in include/scape.h.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "../../include/scape.h"
+#include "scape_kernels.cuh"
+
+#define SCAPE_API extern "C" __attribute__((visibility("default")))
+
+namespace scape {
+int num_sms() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+  }
+  return n;
+}
+}  // namespace scape
+
+using namespace scape;
+
+struct scape_handle {
+  // geometry
+  uint64_t N = 0, Np = 0, n_wt = 0, n_blk = 0, mask_words = 0, mask_alloc = 0;
+  uint32_t C = 0;
+  int W = 0;
+  double density = 0;
+  uint64_t n_ch = 0, q = 0, K = 0, Kp = 0;
+  uint32_t k_full = 0, k_last = 0;
+  // hyper-parameters (fp32, as used)
+  float b1 = 0, b2 = 0, lr = 0, wd = 0, eps = 0, c1 = 0, c2 = 0, invW = 0;
+  // device state
+  float *theta = nullptr, *v = nullptr, *u = nullptr, *e = nullptr;
+  float *vals = nullptr, *bbar = nullptr;
+  uint32_t* idx = nullptr;
+  uint32_t* mask[2] = {nullptr, nullptr};
+  uint32_t *toff_local = nullptr, *bsum = nullptr;
+  uint16_t* stage = nullptr;  // scape_step_host staging, W x N bf16
+  int prev = 0;               // mask[prev] = M_{t-1} for the next step
+  bool has_mask = false;      // a mask exists (built by a step or loaded)
+  bool stepped = false;       // compact buffers hold a step's output
+  int64_t t = 0;
+  cudaStream_t last_stream = nullptr;
+  uint64_t device_bytes = 0;
+  // profiling
+  bool profiling = false;
+  std::vector<cudaEvent_t> ev_pool;
+  std::vector<std::pair<int, std::pair<cudaEvent_t, cudaEvent_t>>> ev_rec;
+  std::string err;
+};
+
+namespace {
+
+thread_local std::string g_create_err;
+
+int fail(scape_handle* h, int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  if (h) h->err = buf; else g_create_err = buf;
+  return code;
+}
+
+int cuda_fail(scape_handle* h, cudaError_t e, const char* what) {
+  return fail(h, SCAPE_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+template <class T>
+cudaError_t dalloc(scape_handle* h, T** p, uint64_t count) {
+  const uint64_t bytes = (count ? count : 1) * sizeof(T);
+  cudaError_t e = cudaMalloc(reinterpret_cast<void**>(p), bytes);
+  if (e == cudaSuccess) {
+    h->device_bytes += bytes;
+    e = cudaMemset(*p, 0, bytes);
+  }
+  return e;
+}
+
+void release(scape_handle* h) {
+  void* ps[] = {h->theta, h->v, h->u, h->e, h->vals, h->bbar, h->idx, h->mask[0], h->mask[1],
+                h->toff_local, h->bsum, h->stage};
+  for (void* p : ps)
+    if (p) cudaFree(p);
+  for (cudaEvent_t ev : h->ev_pool) cudaEventDestroy(ev);
+  for (auto& r : h->ev_rec) {
+    cudaEventDestroy(r.second.first);
+    cudaEventDestroy(r.second.second);
+  }
+}
+
+cudaEvent_t get_event(scape_handle* h) {
+  if (!h->ev_pool.empty()) {
+    cudaEvent_t ev = h->ev_pool.back();
+    h->ev_pool.pop_back();
+    return ev;
+  }
+  cudaEvent_t ev = nullptr;
+  cudaEventCreate(&ev);
+  return ev;
+}
+
+// Records an event pair around one phase when profiling.
+struct PhaseTimer {
+  scape_handle* h;
+  int ph;
+  cudaStream_t s;
+  cudaEvent_t a = nullptr;
+  PhaseTimer(scape_handle* h_, int ph_, cudaStream_t s_) : h(h_), ph(ph_), s(s_) {
+    if (h->profiling) {
+      a = get_event(h);
+      cudaEventRecord(a, s);
+    }
+  }
+  void done() {
+    if (a) {
+      cudaEvent_t b = get_event(h);
+      cudaEventRecord(b, s);
+      h->ev_rec.push_back({ph, {a, b}});
+      a = nullptr;
+    }
+  }
+};
+
+bool is_field(int which) { return which >= SCAPE_THETA && which <= SCAPE_STEP; }
+
+cudaError_t wait_last(scape_handle* h) {
+  return h->last_stream ? cudaStreamSynchronize(h->last_stream) : cudaDeviceSynchronize();
+}
+
+// Checks that a 0/1 bitmap (host copy) carries exactly k_c bits in every chunk
+// and none past N.
+bool mask_valid(const scape_handle* h, const std::vector<uint32_t>& m, std::string& why) {
+  for (uint64_t c = 0; c < h->n_ch; c++) {
+    const uint64_t w0 = c * h->C / 32;
+    const uint64_t len = std::min<uint64_t>(h->C, h->N - c * h->C);
+    const uint64_t nw = (len + 31) / 32;
+    uint64_t cnt = 0;
+    for (uint64_t j = 0; j < nw; j++) cnt += __builtin_popcount(m[w0 + j]);
+    const uint64_t k = c == h->n_ch - 1 ? h->k_last : h->k_full;
+    if (cnt != k) {
+      why = "chunk " + std::to_string(c) + " has " + std::to_string(cnt) + " bits, needs " +
+            std::to_string(k);
+      return false;
+    }
+  }
+  if (h->N % 32) {
+    const uint32_t tail = m[h->mask_words - 1] >> (h->N % 32);
+    if (tail) {
+      why = "bits set past the last coordinate";
+      return false;
+    }
+  }
+  return true;
+}
+
+}  // namespace
+
+SCAPE_API int scape_create(const scape_layout* layout, int W, double density, float beta1,
+                           float beta2, float lr, float wd, float eps, scape_handle** out) {
+  if (!out) return fail(nullptr, SCAPE_EINVAL, "out is NULL");
+  *out = nullptr;
+  if (!layout || !layout->numel || layout->n_tensors == 0)
+    return fail(nullptr, SCAPE_EINVAL, "layout must list at least one tensor");
+  if (W < 1 || W > kMaxW) return fail(nullptr, SCAPE_EINVAL, "W=%d outside [1, %d]", W, kMaxW);
+  if (!(density > 0.0 && density <= 1.0))
+    return fail(nullptr, SCAPE_EINVAL, "density %g outside (0, 1]", density);
+  const uint32_t C = layout->chunk;
+  if (C < 32 || C > kMaxChunk || C % 32)
+    return fail(nullptr, SCAPE_EINVAL, "chunk %u must be a multiple of 32 in [32, %u]", C,
+                kMaxChunk);
+  uint64_t N = 0;
+  for (uint32_t i = 0; i < layout->n_tensors; i++) {
+    if (layout->numel[i] > (1ull << 32)) return fail(nullptr, SCAPE_EINVAL, "tensor too large");
+    N += layout->numel[i];
+  }
+  if (N == 0 || N >= (1ull << 32))
+    return fail(nullptr, SCAPE_EINVAL, "N=%llu must be in [1, 2^32)", (unsigned long long)N);
+  if (!std::isfinite(beta1) || !std::isfinite(beta2) || !std::isfinite(lr) ||
+      !std::isfinite(wd) || !(eps > 0.0f) || !std::isfinite(eps))
+    return fail(nullptr, SCAPE_EINVAL, "hyper-parameters must be finite and eps > 0");
+
+  scape_handle* h = new (std::nothrow) scape_handle();
+  if (!h) return fail(nullptr, SCAPE_ENOMEM, "host allocation failed");
+  h->N = N;
+  h->C = C;
+  h->W = W;
+  h->density = density;
+  h->b1 = beta1; h->b2 = beta2; h->lr = lr; h->wd = wd; h->eps = eps;
+  h->c1 = 1.0f - beta1;
+  h->c2 = 1.0f - beta2;
+  h->invW = 1.0f / (float)W;
+  h->Np = (N + kTile - 1) / kTile * kTile;
+  h->n_wt = h->Np / kTile;
+  h->n_blk = (h->n_wt + kTilesPerBlk - 1) / kTilesPerBlk;
+  h->mask_words = (N + 31) / 32;
+  h->mask_alloc = h->n_wt * 8;
+  h->n_ch = (N + C - 1) / C;
+  h->q = (h->n_ch + W - 1) / W;
+  h->k_full = (uint32_t)std::floor(density * (double)C);
+  const uint64_t last_len = N - (h->n_ch - 1) * C;
+  h->k_last = (uint32_t)std::floor(density * (double)last_len);
+  h->K = (h->n_ch - 1) * (uint64_t)h->k_full + h->k_last;
+  h->Kp = (h->K + 3) / 4 * 4;
+
+  cudaError_t e = cudaSuccess;
+  if (e == cudaSuccess) e = dalloc(h, &h->theta, h->Np);
+  if (e == cudaSuccess) e = dalloc(h, &h->v, h->Np);
+  if (e == cudaSuccess) e = dalloc(h, &h->u, (uint64_t)W * h->Np);
+  if (e == cudaSuccess) e = dalloc(h, &h->e, (uint64_t)W * h->Np);
+  if (e == cudaSuccess) e = dalloc(h, &h->vals, (uint64_t)W * h->Kp);
+  if (e == cudaSuccess) e = dalloc(h, &h->bbar, h->Kp);
+  if (e == cudaSuccess) e = dalloc(h, &h->idx, h->Kp);
+  if (e == cudaSuccess) e = dalloc(h, &h->mask[0], h->mask_alloc);
+  if (e == cudaSuccess) e = dalloc(h, &h->mask[1], h->mask_alloc);
+  if (e == cudaSuccess) e = dalloc(h, &h->toff_local, h->n_wt);
+  if (e == cudaSuccess) e = dalloc(h, &h->bsum, h->n_blk);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) {
+    const int code = (e == cudaErrorMemoryAllocation) ? SCAPE_ENOMEM : SCAPE_ECUDA;
+    fail(nullptr, code, "device allocation of %.3f GB failed: %s",
+         (double)h->device_bytes / 1e9, cudaGetErrorString(e));
+    cudaGetLastError();
+    release(h);
+    delete h;
+    return code;
+  }
+  *out = h;
+  return SCAPE_OK;
+}
+
+SCAPE_API void scape_destroy(scape_handle* h) {
+  if (!h) return;
+  wait_last(h);
+  release(h);
+  delete h;
+}
+
+SCAPE_API const char* scape_last_error(const scape_handle* h) {
+  return h ? h->err.c_str() : g_create_err.c_str();
+}
+
+SCAPE_API int scape_info(const scape_handle* h, scape_info_t* out) {
+  if (!h || !out) return SCAPE_EINVAL;
+  out->N = h->N;
+  out->W = (uint32_t)h->W;
+  out->chunk = h->C;
+  out->n_chunks = h->n_ch;
+  out->chunks_per_worker = h->q;
+  out->k_full = h->k_full;
+  out->k_last = h->k_last;
+  out->K = h->K;
+  out->mask_words = h->mask_words;
+  out->step = h->t;
+  out->device_bytes = h->device_bytes;
+  return SCAPE_OK;
+}
+
+static int step_device(scape_handle* h, const uint16_t* const* g, cudaStream_t s) {
+  cudaError_t e;
+  uint32_t* mprev = h->mask[h->prev];
+  uint32_t* mcur = h->mask[1 - h->prev];
+
+  SelectArgs sa{};
+  for (int w = 0; w < h->W; w++) sa.grads[w] = g[w];
+  sa.e = h->e;
+  sa.u = h->u;
+  sa.vals = h->vals;
+  sa.b1 = h->b1;
+  sa.c1 = h->c1;
+  sa.N = h->N;
+  sa.Np = h->Np;
+  sa.Kp = h->Kp;
+  sa.n_ch = h->n_ch;
+  sa.q = h->q;
+  sa.C = h->C;
+  sa.k_full = h->k_full;
+  sa.k_last = h->k_last;
+
+  if (!h->has_mask) {  // step 0: M_{-1} from the step-0 accumulators
+    PhaseTimer pt(h, SCAPE_PH_SELECT_BOOT, s);
+    sa.mprev = nullptr;
+    sa.mout = mprev;
+    if ((e = launch_select(sa, true, s)) != cudaSuccess) return cuda_fail(h, e, "select (step 0)");
+    pt.done();
+  }
+  {
+    PhaseTimer pt(h, SCAPE_PH_OFFSETS, s);
+    if ((e = launch_offsets(mprev, h->toff_local, h->bsum, h->n_wt, s)) != cudaSuccess)
+      return cuda_fail(h, e, "offsets");
+    pt.done();
+  }
+  {
+    StreamArgs a{};
+    for (int w = 0; w < h->W; w++) a.grads[w] = g[w];
+    a.u = h->u;
+    a.e = h->e;
+    a.vals = h->vals;
+    a.mprev = mprev;
+    a.toff_local = h->toff_local;
+    a.bsum = h->bsum;
+    a.N = h->N;
+    a.Np = h->Np;
+    a.Kp = h->Kp;
+    a.n_wt = h->n_wt;
+    a.b1 = h->b1;
+    a.c1 = h->c1;
+    PhaseTimer pt(h, SCAPE_PH_STREAM, s);
+    if ((e = launch_stream_compact(a, h->W, s)) != cudaSuccess)
+      return cuda_fail(h, e, "stream_compact");
+    pt.done();
+  }
+  {
+    UpdateArgs a{};
+    a.theta = h->theta;
+    a.v = h->v;
+    a.vals = h->vals;
+    a.bbar = h->bbar;
+    a.idx = h->idx;
+    a.mprev = mprev;
+    a.toff_local = h->toff_local;
+    a.bsum = h->bsum;
+    a.N = h->N;
+    a.Kp = h->Kp;
+    a.n_wt = h->n_wt;
+    a.W = h->W;
+    a.b2 = h->b2;
+    a.c2 = h->c2;
+    a.lr = h->lr;
+    a.wd = h->wd;
+    a.eps = h->eps;
+    a.invW = h->invW;
+    PhaseTimer pt(h, SCAPE_PH_UPDATE, s);
+    if ((e = launch_reduce_update(a, s)) != cudaSuccess) return cuda_fail(h, e, "reduce_update");
+    pt.done();
+  }
+  {
+    sa.mprev = mprev;
+    sa.mout = mcur;
+    PhaseTimer pt(h, SCAPE_PH_SELECT, s);
+    if ((e = launch_select(sa, false, s)) != cudaSuccess) return cuda_fail(h, e, "select");
+    pt.done();
+  }
+  h->prev = 1 - h->prev;
+  h->has_mask = true;
+  h->stepped = true;
+  h->t += 1;
+  h->last_stream = s;
+  return SCAPE_OK;
+}
+
+static int check_grad_ptrs(scape_handle* h, const void* const* gp, bool device) {
+  if (!gp) return fail(h, SCAPE_EINVAL, "grad_ptrs is NULL");
+  for (int w = 0; w < h->W; w++) {
+    if (!gp[w]) return fail(h, SCAPE_EINVAL, "grad_ptrs[%d] is NULL", w);
+    if (device && (reinterpret_cast<uintptr_t>(gp[w]) & 15))
+      return fail(h, SCAPE_EINVAL, "grad_ptrs[%d] is not 16-byte aligned", w);
+  }
+  return SCAPE_OK;
+}
+
+SCAPE_API int scape_step(scape_handle* h, const void* const* grad_ptrs, void* stream) {
+  if (!h) return SCAPE_EINVAL;
+  int rc = check_grad_ptrs(h, grad_ptrs, true);
+  if (rc) return rc;
+  std::vector<const uint16_t*> g(h->W);
+  for (int w = 0; w < h->W; w++) g[w] = static_cast<const uint16_t*>(grad_ptrs[w]);
+  return step_device(h, g.data(), static_cast<cudaStream_t>(stream));
+}
+
+SCAPE_API int scape_step_host(scape_handle* h, const void* const* host_grad_ptrs, void* stream) {
+  if (!h) return SCAPE_EINVAL;
+  int rc = check_grad_ptrs(h, host_grad_ptrs, false);
+  if (rc) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  const uint64_t per = (h->N + 7) / 8 * 8;  // keep every worker's slice 16-byte aligned
+  if (!h->stage) {
+    if ((e = cudaMalloc(&h->stage, (uint64_t)h->W * per * sizeof(uint16_t))) != cudaSuccess) {
+      h->stage = nullptr;
+      cudaGetLastError();
+      return fail(h, e == cudaErrorMemoryAllocation ? SCAPE_ENOMEM : SCAPE_ECUDA,
+                  "staging allocation failed: %s", cudaGetErrorString(e));
+    }
+    h->device_bytes += (uint64_t)h->W * per * sizeof(uint16_t);
+  }
+  std::vector<const uint16_t*> g(h->W);
+  {
+    PhaseTimer pt(h, SCAPE_PH_H2D, s);
+    for (int w = 0; w < h->W; w++) {
+      uint16_t* dst = h->stage + (uint64_t)w * per;
+      if ((e = cudaMemcpyAsync(dst, host_grad_ptrs[w], h->N * sizeof(uint16_t),
+                               cudaMemcpyHostToDevice, s)) != cudaSuccess)
+        return cuda_fail(h, e, "gradient copy");
+      g[w] = dst;
+    }
+    pt.done();
+  }
+  return step_device(h, g.data(), s);
+}
+
+SCAPE_API int scape_mask(scape_handle* h, uint32_t* out_bits) {
+  if (!h) return SCAPE_EINVAL;
+  if (!out_bits) return fail(h, SCAPE_EINVAL, "out_bits is NULL");
+  if (!h->has_mask) return fail(h, SCAPE_ESTATE, "no mask before the first step");
+  cudaError_t e = wait_last(h);
+  if (e == cudaSuccess)
+    e = cudaMemcpy(out_bits, h->mask[h->prev], h->mask_words * 4, cudaMemcpyDefault);
+  return e == cudaSuccess ? SCAPE_OK : cuda_fail(h, e, "scape_mask");
+}
+
+static int field_ptr(scape_handle* h, int which, int w, char** base, uint64_t* count,
+                     uint64_t* esize) {
+  if (!is_field(which)) return fail(h, SCAPE_EINVAL, "unknown state field %d", which);
+  if ((which == SCAPE_U || which == SCAPE_E) && (w < 0 || w >= h->W))
+    return fail(h, SCAPE_EINVAL, "worker %d outside [0, %d)", w, h->W);
+  switch (which) {
+    case SCAPE_THETA: *base = (char*)h->theta; *count = h->N; *esize = 4; break;
+    case SCAPE_V: *base = (char*)h->v; *count = h->N; *esize = 4; break;
+    case SCAPE_U: *base = (char*)(h->u + (uint64_t)w * h->Np); *count = h->N; *esize = 4; break;
+    case SCAPE_E: *base = (char*)(h->e + (uint64_t)w * h->Np); *count = h->N; *esize = 4; break;
+    case SCAPE_MASK: *base = (char*)h->mask[h->prev]; *count = h->mask_words; *esize = 4; break;
+    default: *base = nullptr; *count = 1; *esize = 8; break;
+  }
+  return SCAPE_OK;
+}
+
+SCAPE_API int scape_read_state(scape_handle* h, int which, int w, void* dst, uint64_t offset,
+                               uint64_t count) {
+  if (!h) return SCAPE_EINVAL;
+  if (!dst) return fail(h, SCAPE_EINVAL, "dst is NULL");
+  char* base;
+  uint64_t n, es;
+  int rc = field_ptr(h, which, w, &base, &n, &es);
+  if (rc) return rc;
+  if (offset > n || count > n - offset) return fail(h, SCAPE_EINVAL, "range outside the field");
+  cudaError_t e = wait_last(h);
+  if (e != cudaSuccess) return cuda_fail(h, e, "scape_read_state");
+  if (which == SCAPE_STEP) {
+    int64_t t = h->t;
+    e = cudaMemcpy(dst, &t, 8, cudaMemcpyDefault);
+  } else {
+    e = cudaMemcpy(dst, base + offset * es, count * es, cudaMemcpyDefault);
+  }
+  return e == cudaSuccess ? SCAPE_OK : cuda_fail(h, e, "scape_read_state");
+}
+
+SCAPE_API int scape_load_state(scape_handle* h, int which, int w, const void* src, uint64_t offset,
+                               uint64_t count) {
+  if (!h) return SCAPE_EINVAL;
+  if (!src) return fail(h, SCAPE_EINVAL, "src is NULL");
+  char* base;
+  uint64_t n, es;
+  int rc = field_ptr(h, which, w, &base, &n, &es);
+  if (rc) return rc;
+  if (offset > n || count > n - offset) return fail(h, SCAPE_EINVAL, "range outside the field");
+  cudaError_t e = wait_last(h);
+  if (e != cudaSuccess) return cuda_fail(h, e, "scape_load_state");
+  if (which == SCAPE_STEP) {
+    int64_t t;
+    if ((e = cudaMemcpy(&t, src, 8, cudaMemcpyDefault)) != cudaSuccess)
+      return cuda_fail(h, e, "scape_load_state");
+    if (t < 0) return fail(h, SCAPE_EINVAL, "step must be >= 0");
+    h->t = t;
+    return SCAPE_OK;
+  }
+  if (which == SCAPE_MASK) {
+    if (offset != 0 || count != h->mask_words)
+      return fail(h, SCAPE_EINVAL, "a mask load must cover all %llu words",
+                  (unsigned long long)h->mask_words);
+    std::vector<uint32_t> m(count);
+    if ((e = cudaMemcpy(m.data(), src, count * 4, cudaMemcpyDefault)) != cudaSuccess)
+      return cuda_fail(h, e, "scape_load_state");
+    std::string why;
+    if (!mask_valid(h, m, why)) return fail(h, SCAPE_EINVAL, "invalid mask: %s", why.c_str());
+    if ((e = cudaMemcpy(base, m.data(), count * 4, cudaMemcpyHostToDevice)) != cudaSuccess)
+      return cuda_fail(h, e, "scape_load_state");
+    h->has_mask = true;
+    return SCAPE_OK;
+  }
+  e = cudaMemcpy(base + offset * es, src, count * es, cudaMemcpyDefault);
+  return e == cudaSuccess ? SCAPE_OK : cuda_fail(h, e, "scape_load_state");
+}
+
+SCAPE_API int scape_read_sparse(scape_handle* h, int w, uint32_t* idx, float* vals,
+                                uint64_t offset, uint64_t count, uint64_t* total) {
+  if (!h) return SCAPE_EINVAL;
+  if (w < -1 || w >= h->W) return fail(h, SCAPE_EINVAL, "worker %d outside [-1, %d)", w, h->W);
+  if (total) *total = h->K;
+  if (!h->stepped) return fail(h, SCAPE_ESTATE, "no step has run");
+  if (offset > h->K || count > h->K - offset) return fail(h, SCAPE_EINVAL, "range outside [0, K)");
+  cudaError_t e = wait_last(h);
+  if (e == cudaSuccess && idx && count)
+    e = cudaMemcpy(idx, h->idx + offset, count * 4, cudaMemcpyDefault);
+  if (e == cudaSuccess && vals && count) {
+    const float* src = w < 0 ? h->bbar : h->vals + (uint64_t)w * h->Kp;
+    e = cudaMemcpy(vals, src + offset, count * 4, cudaMemcpyDefault);
+  }
+  return e == cudaSuccess ? SCAPE_OK : cuda_fail(h, e, "scape_read_sparse");
+}
+
+SCAPE_API int scape_profile(scape_handle* h, int enable) {
+  if (!h) return SCAPE_EINVAL;
+  h->profiling = enable != 0;
+  return SCAPE_OK;
+}
+
+SCAPE_API int scape_profile_read(scape_handle* h, double* ms, uint32_t* launches) {
+  if (!h) return SCAPE_EINVAL;
+  if (ms)
+    for (int i = 0; i < SCAPE_N_PHASES; i++) ms[i] = 0;
+  if (launches)
+    for (int i = 0; i < SCAPE_N_PHASES; i++) launches[i] = 0;
+  for (auto& r : h->ev_rec) {
+    cudaError_t e = cudaEventSynchronize(r.second.second);
+    float t = 0;
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&t, r.second.first, r.second.second);
+    if (e != cudaSuccess) return cuda_fail(h, e, "scape_profile_read");
+    if (ms) ms[r.first] += t;
+    if (launches) launches[r.first] += 1;
+    h->ev_pool.push_back(r.second.first);
+    h->ev_pool.push_back(r.second.second);
+  }
+  h->ev_rec.clear();
+  return SCAPE_OK;
+}

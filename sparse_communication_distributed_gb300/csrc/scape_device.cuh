@@ -1,0 +1,56 @@
+// Device helpers shared by the libscape kernels (internal).
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace scape {
+
+constexpr unsigned kFull = 0xFFFFFFFFu;
+
+__device__ __forceinline__ uint32_t warp_incl_scan(uint32_t x, int lane) {
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    uint32_t y = __shfl_up_sync(kFull, x, d);
+    if (lane >= d) x += y;
+  }
+  return x;
+}
+
+// Block-wide inclusive scan of one value per thread; "warp_tot" is shared
+// scratch of at least blockDim.x/32 + 1 entries.  Returns the inclusive
+// prefix; *total receives the block total.  Contains __syncthreads().
+template <int NT>
+__device__ __forceinline__ uint32_t block_incl_scan(uint32_t x, uint32_t* warp_tot,
+                                                    uint32_t* total) {
+  constexpr int NW = NT / 32;
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  uint32_t inc = warp_incl_scan(x, lane);
+  if (lane == 31) warp_tot[wid] = inc;
+  __syncthreads();
+  if (wid == 0) {
+    uint32_t t = lane < NW ? warp_tot[lane] : 0u;
+    uint32_t ti = warp_incl_scan(t, lane);
+    if (lane < NW) warp_tot[lane] = ti - t;  // exclusive warp offsets
+    if (lane == NW - 1) warp_tot[NW] = ti;
+  }
+  __syncthreads();
+  uint32_t r = inc + warp_tot[wid];
+  *total = warp_tot[NW];
+  __syncthreads();
+  return r;
+}
+
+__device__ __forceinline__ float bf16lo(uint32_t x) { return __uint_as_float(x << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t x) { return __uint_as_float(x & 0xFFFF0000u); }
+__device__ __forceinline__ float bf16f(uint16_t h) { return __uint_as_float((uint32_t)h << 16); }
+
+// Streaming 16-byte load that is not kept in L1 (read-once data).
+__device__ __forceinline__ uint4 ld_stream_u4(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+}  // namespace scape

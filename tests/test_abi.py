@@ -1,0 +1,80 @@
+"""The C ABI without a GPU: libscape.so loads, exports every entry point that
+include/scape.h declares, and rejects bad arguments before touching CUDA."""
+import ctypes
+import os
+import re
+import subprocess
+
+import numpy as np
+import pytest
+
+import sparse_communication_distributed_gb300 as pkg
+from sparse_communication_distributed_gb300 import build, scape
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(scape.LIB_PATH):
+        build.build()
+    return scape.load_library()
+
+
+def declared():
+    txt = open(os.path.join(ROOT, "include", "scape.h")).read()
+    return sorted(set(re.findall(r"^\s*(?:int|void|const char\*)\s+(scape_\w+)\(", txt, re.M)))
+
+
+def test_header_matches_binding():
+    assert declared() == sorted(scape.EXPORTS)
+
+
+def test_exports_every_declared_symbol(lib):
+    for name in declared():
+        assert hasattr(lib, name), name
+    out = subprocess.run(["nm", "-D", "--defined-only", scape.LIB_PATH], capture_output=True,
+                         text=True).stdout
+    exported = set(re.findall(r" T (scape_\w+)$", out, re.M))
+    assert exported == set(declared()), exported ^ set(declared())
+
+
+def _create(lib, numel, chunk, W, density, eps=1e-8):
+    arr = np.asarray(numel, np.uint64)
+    lay = scape._Layout(arr.size, arr.ctypes.data_as(ctypes.POINTER(ctypes.c_uint64)), chunk)
+    h = ctypes.c_void_p(1234)
+    rc = lib.scape_create(ctypes.byref(lay), W, density, 0.9, 0.95, 1e-3, 0.1, eps, ctypes.byref(h))
+    return rc, h
+
+
+@pytest.mark.parametrize("numel,chunk,W,density,eps,what", [
+    ([1024], 1024, 0, 0.1, 1e-8, "W=0"),
+    ([1024], 1024, 65, 0.1, 1e-8, "W=65"),
+    ([1024], 1024, 2, 0.0, 1e-8, "density"),
+    ([1024], 1024, 2, 1.5, 1e-8, "density"),
+    ([1024], 48, 2, 0.1, 1e-8, "chunk"),
+    ([1024], 131072, 2, 0.1, 1e-8, "chunk"),
+    ([0], 1024, 2, 0.1, 1e-8, "N="),
+    ([1 << 31, 1 << 31], 1024, 2, 0.1, 1e-8, "N="),
+    ([1024], 1024, 2, 0.1, 0.0, "eps"),
+])
+def test_create_rejects_bad_arguments(lib, numel, chunk, W, density, eps, what):
+    rc, h = _create(lib, numel, chunk, W, density, eps)
+    assert rc == scape.SCAPE_EINVAL
+    assert not h.value
+    assert what in lib.scape_last_error(None).decode()
+
+
+def test_null_handles(lib):
+    lib.scape_destroy(None)
+    assert lib.scape_step(None, None, None) == scape.SCAPE_EINVAL
+    assert lib.scape_mask(None, None) == scape.SCAPE_EINVAL
+    assert lib.scape_info(None, None) == scape.SCAPE_EINVAL
+    assert lib.scape_read_sparse(None, 0, None, None, 0, 0, None) == scape.SCAPE_EINVAL
+
+
+def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
+    monkeypatch.setattr(scape, "_lib", None)
+    with pytest.raises(ImportError):
+        scape.load_library(str(tmp_path / "missing.so"))
+    assert pkg.Scape is scape.Scape

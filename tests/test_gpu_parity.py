@@ -1,0 +1,183 @@
+"""libscape against the oracle, element by element, on the same seeded inputs.
+
+- the 2^20 workload (W=4, density 0.10, chunk 4096, 5 steps) over every
+  coordinate and every step;
+- edge cases: ragged sizes (N not a multiple of 8, 32 or 256), the smallest
+  chunk, W = 1 and odd W, density 1 and densities giving k = 0, all-equal
+  accumulators, heavy ties in a 65536 chunk (more candidates than the
+  shared-memory list holds), +-0;
+- the full-size workloads in the launch configuration the bench times, on
+  sampled whole chunks (both ends, every shard boundary, seeded others),
+  plus properties over every chunk.
+"""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+import oracle  # noqa: E402
+import synth  # noqa: E402
+from gpu_harness import GpuRun, OracleRun, check_full_mask, compare, sample_chunks  # noqa: E402
+from sparse_communication_distributed_gb300 import E, MASK, STEP, THETA, U, V, Scape  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+
+def _run_both(wl, density, steps, chunk_ids=None, every=True):
+    g = GpuRun(wl, density)
+    r = OracleRun(wl, density, chunk_ids=chunk_ids)
+    try:
+        for t in range(steps):
+            g.step()
+            r.step()
+            if every or t == steps - 1:
+                compare(g, r, f"step {t}")
+        check_full_mask(g)
+    finally:
+        g.close()
+
+
+def test_flat_2p20_every_coordinate():
+    wl = synth.WORKLOADS["flat-2^20-w4"]
+    _run_both(wl, wl.densities[0], wl.steps)
+
+
+@pytest.mark.parametrize("N,W,chunk,density", [
+    (1000, 1, 32, 0.1),        # N % 8 != 0, k = 3, single worker
+    (4099, 3, 96, 0.05),       # chunk not a power of two, ragged tail, odd W
+    (70001, 5, 1024, 0.01),    # k = 10, last chunk 369 -> k = 3
+    (3000, 2, 64, 0.01),       # k = 0 everywhere
+    (2048 + 7, 4, 512, 1.0),   # density 1: every coordinate, dense AdamS
+    (65536 * 2 + 160, 2, 65536, 0.3),  # large k in a full chunk, 160-coordinate last chunk
+])
+def test_edge_shapes(N, W, chunk, density):
+    wl = synth.tiny(N, W, chunk, density, seed=N)
+    _run_both(wl, density, 4)
+
+
+def test_heavy_ties_overflow_candidates():
+    # Student-t means on a 2^-14 grid: |a| takes few hundred values, so the bin
+    # holding the threshold exceeds the shared-memory candidate list.
+    wl = synth.tiny(65536 * 3, 3, 65536, 0.1, kind=synth.SYN_STUDENT_Q, seed=3)
+    _run_both(wl, 0.1, 4)
+
+
+def _const_grads(wl, value):
+    bits = np.float32(value).view(np.uint32) >> 16
+    return np.full((wl.W, wl.N), bits, np.uint16)
+
+
+def test_all_equal_accumulators():
+    # constant gradient: every |a| in a chunk is equal, the first k coordinates win
+    wl = synth.tiny(8192 + 96, 2, 4096, 0.1)
+    g, r = GpuRun(wl, 0.1), OracleRun(wl, 0.1)
+    try:
+        for t in range(3):
+            gr = _const_grads(wl, -0.0625)
+            g.step(gr)
+            r.step(gr)
+            compare(g, r, f"step {t}")
+        bits = np.unpackbits(g.sc.mask().view(np.uint8), bitorder="little")
+        assert bits[:409].all() and not bits[409:4096].any()
+    finally:
+        g.close()
+
+
+def test_loaded_residuals_select_exactly():
+    # beta1 = 0 makes u = g; with zero gradients a = e, so both selections of a
+    # step (step 0 and the new mask) rank the loaded e: +-0, ties, denormals.
+    wl = synth.tiny(4 * 1024, 2, 1024, 0.25, beta1=0.0)
+    rng = np.random.default_rng(5)
+    e0 = (rng.integers(-8, 9, (2, wl.N)) * 0.5).astype(np.float32)
+    e0[:, ::97] = -0.0
+    e0[:, 5::131] = np.float32(1e-40)
+    g, r = GpuRun(wl, 0.25), OracleRun(wl, 0.25)
+    try:
+        for w in range(2):
+            g.sc.load(E, e0[w], w)
+            r.o.set(oracle.E, e0[w], w)
+        zero = np.zeros((2, wl.N), np.uint16)
+        for t in range(2):
+            g.step(zero)
+            r.step(zero)
+            compare(g, r, f"step {t}")
+    finally:
+        g.close()
+
+
+def test_resume_is_bit_identical():
+    wl = synth.tiny(3 * 4096 + 32, 3, 4096, 0.05, seed=8)
+    a = GpuRun(wl, 0.05)
+    for _ in range(5):
+        a.step()
+    ref = {f: a.sc.read(f) for f in (THETA, V, MASK)}
+    ref_u = [a.sc.read(U, w) for w in range(3)]
+    a.close()
+    b = GpuRun(wl, 0.05)
+    for _ in range(3):
+        b.step()
+    saved = {f: b.sc.read(f) for f in (THETA, V, MASK, STEP)}
+    saved_ue = [(b.sc.read(U, w), b.sc.read(E, w)) for w in range(3)]
+    b.close()
+    c = GpuRun(wl, 0.05, theta0=False)
+    for f in (THETA, V, MASK, STEP):
+        c.sc.load(f, saved[f])
+    for w in range(3):
+        c.sc.load(U, saved_ue[w][0], w)
+        c.sc.load(E, saved_ue[w][1], w)
+    c.t = 3
+    for _ in range(2):
+        c.step()
+    try:
+        for f in (THETA, V, MASK):
+            assert np.array_equal(c.sc.read(f).view(np.uint32), ref[f].view(np.uint32)), f
+        for w in range(3):
+            assert np.array_equal(c.sc.read(U, w).view(np.uint32), ref_u[w].view(np.uint32))
+        assert int(c.sc.read(STEP)[0]) == 5
+    finally:
+        c.close()
+
+
+def test_step_host_matches_step():
+    wl = synth.tiny(20000, 2, 1024, 0.1, seed=4)
+    a, b = GpuRun(wl, 0.1), GpuRun(wl, 0.1)
+    try:
+        for t in range(3):
+            gr = np.stack([synth.cpu().grads(wl, w, t, n=wl.N) for w in range(2)])
+            a.step(gr)
+            pinned = [torch.from_numpy(gr[w].view(np.int16)).pin_memory() for w in range(2)]
+            b.sc.step_host(pinned)
+        torch.cuda.synchronize()
+        for f in (THETA, V, MASK):
+            assert np.array_equal(a.sc.read(f).view(np.uint32), b.sc.read(f).view(np.uint32))
+    finally:
+        a.close()
+        b.close()
+
+
+def test_generator_gpu_equals_cpu():
+    for name in ("flat-2^26-w8-ties", "gpt2-medium-w8", "llama-1.8b-w4"):
+        wl = synth.WORKLOADS[name]
+        n = 1 << 16
+        for i0 in (0, wl.N // 2 + 5, wl.N - n):
+            buf = torch.empty(n, dtype=torch.int16, device="cuda")
+            synth.gpu().grads_into(wl, 1, 7, buf, i0=i0)
+            ref = synth.cpu().grads(wl, 1, 7, i0=i0, n=n)
+            assert np.array_equal(buf.cpu().numpy().view(np.uint16), ref), (name, i0)
+        th = torch.empty(n, dtype=torch.float32, device="cuda")
+        synth.gpu().theta_into(wl, th, i0=12345)
+        ref = synth.cpu().theta0(wl, np.arange(12345, 12345 + n))
+        assert np.array_equal(th.cpu().numpy().view(np.uint32), ref.view(np.uint32))
+
+
+FULL = [("flat-2^26-w8-ties", 0.10), ("flat-2^26-w8-ties", 0.01), ("gpt2-medium-w8", 0.01),
+        ("llama-500m-w8", 0.01), ("llama-500m-w8", 0.10), ("llama-1.8b-w4", 0.01)]
+
+
+@pytest.mark.parametrize("name,density", FULL, ids=[f"{n}-d{d}" for n, d in FULL])
+def test_full_size_sampled_chunks(name, density):
+    wl = synth.WORKLOADS[name]
+    ids = sample_chunks(wl)
+    _run_both(wl, density, wl.steps, chunk_ids=ids)
