@@ -116,6 +116,12 @@ WORKLOADS = {
                     "chunk 65536, 10 steps"),
 }
 
+# A small flat layout for profiler captures: state and gradients ~2 GB on the
+# device (well above L2), same per-worker shape as the 1.8B layout.
+WORKLOADS["profile-2^25-w4"] = Workload(
+    "profile-2^25-w4", (("flat", (1 << 25,)),), W=4, chunk=65536, densities=(0.01,), steps=3,
+    sigma=1e-3, description="one tensor of 2^25, W=4, density 0.01, chunk 65536 (profiling case)")
+
 # The workload the throughput line is quoted on.
 BENCH_WORKLOAD = "llama-1.8b-w4"
 
