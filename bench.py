@@ -64,15 +64,12 @@ def measured_peak():
 
 
 def alg_bytes(N: int, W: int, K: int) -> dict:
-    """Algorithmic (compulsory) HBM bytes per step and per kernel.
-    stream_compact: W*N*(2 g + 8 u + 8 e + 1/8 mask) + W*K*4 (kept values written)
-    reduce_update:  N*(8 theta + 8 v + 1/8 mask) + K*(4W vals read + 4 bbar + 4 idx)
-    select:         N*(1/8 new mask)  (+4 B/param re-read of a, not counted)
-    """
-    a = W * N * (2 + 8 + 8 + 0.125) + W * K * 4
-    b = N * (8 + 8 + 0.125) + K * (4 * W + 8)
-    c = N * 0.125
-    return {"stream_compact": a, "reduce_update": b, "select": c, "step": a + b + c}
+    """Algorithmic (compulsory) HBM bytes of one step, all in the fused step kernel:
+    per coordinate W*(2 g + 8 u + 8 e + 1/8 applied mask) + 8 theta + 8 v + 1/8 new mask,
+    per kept coordinate W*(4 write + 4 read) of the compact values + 4 bbar + 4 idx.
+    (The owner's accumulator is ranked on-chip, so it is not read back.)"""
+    step = N * (W * (2 + 8 + 8 + 0.125) + 8 + 8 + 0.125) + K * (8 * W + 8)
+    return {"step": step}
 
 
 class ClockSampler:
@@ -125,7 +122,7 @@ class ClockSampler:
 def ncu_traffic(kernel: str, workload: str):
     """Per-launch DRAM bytes from the committed ncu summary, if it was taken on
     the current source of the kernel (else None)."""
-    src = {"stream_compact": "k_stream.cu"}.get(kernel)
+    src = {"step_chunks": "k_fused.cu"}.get(kernel)
     path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
     if not src or not os.path.exists(path):
         return None
@@ -283,9 +280,9 @@ def run_scape(args, wl, density):
         return
     peak, peak_kind = measured_peak()
     ab = alg_bytes(N, W, K)
-    a_ms, a_n = phases["stream_compact"]
+    a_ms, a_n = phases["step"]
     a_launch_ms = a_ms / max(a_n, 1)
-    achieved = ab["stream_compact"] / (a_launch_ms * 1e-3) / 1e9
+    achieved = ab["step"] / (a_launch_ms * 1e-3) / 1e9
     step_gbs = ab["step"] / (ms_per_step * 1e-3) / 1e9
     line = {
         "metric": METRIC,
@@ -308,13 +305,14 @@ def run_scape(args, wl, density):
         "step_hbm": {"alg_bytes_per_step": ab["step"], "achieved_gbs": step_gbs,
                      "frac_of_8tbs": step_gbs / NOMINAL_HBM_GBS,
                      "frac_of_peak": step_gbs / peak, "peak_kind": peak_kind},
-        "roofline": {"kernel": "stream_compact", "bound": "hbm", "achieved": achieved,
+        "roofline": {"kernel": "step_chunks", "bound": "hbm", "achieved": achieved,
                      "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": ncu_traffic("stream_compact", wl.name),
-                     "alg_bytes_per_launch": ab["stream_compact"], "launch_ms": a_launch_ms,
+                     "traffic": ncu_traffic("step_chunks", wl.name),
+                     "alg_bytes_per_launch": ab["step"], "launch_ms": a_launch_ms,
                      "peak_kind": f"{peak_kind} (hbm_gbs)"},
         "kernels_ms_per_step": {k: v[0] / args.steps for k, v in phases.items() if v[1]},
-        "gpu_launches": args.steps * 5,
+        "gpu_launches": args.steps * 2,
+        "select_fallback_chunks": sc._info()["select_fallbacks"],
         "clocks": clk,
         "e2e": e2e,
         "cpu_baseline": cpu,

@@ -75,13 +75,11 @@ enum { SCAPE_THETA = 0, SCAPE_V = 1, SCAPE_U = 2, SCAPE_E = 3, SCAPE_MASK = 4, S
 
 /* Kernel phases reported by scape_profile_read. */
 enum {
-  SCAPE_PH_SELECT_BOOT = 0, /* step 0 only: M_{-1} from the step-0 accumulators */
-  SCAPE_PH_OFFSETS = 1,     /* prefix counts of M_{t-1} (compaction offsets) */
-  SCAPE_PH_STREAM = 2,      /* momentum, accumulate, mask-apply, residual, compaction */
-  SCAPE_PH_UPDATE = 3,      /* fixed-order W-way sum, second moment, AdamS update */
-  SCAPE_PH_SELECT = 4,      /* partitioned per-chunk top-k -> M_t */
-  SCAPE_PH_H2D = 5,         /* scape_step_host: host -> device gradient copies */
-  SCAPE_N_PHASES = 6
+  SCAPE_PH_SELECT_BOOT = 0,     /* step 0 only: M_{-1} from the step-0 accumulators */
+  SCAPE_PH_STEP = 1,            /* the fused step: every rule line, chunk by chunk, incl. M_t */
+  SCAPE_PH_SELECT_FALLBACK = 2, /* standalone top-k of chunks with too many tied keys */
+  SCAPE_PH_H2D = 3,             /* scape_step_host: host -> device gradient copies */
+  SCAPE_N_PHASES = 4
 };
 
 typedef struct {
@@ -96,6 +94,8 @@ typedef struct {
   uint64_t mask_words; /* ceil(N / 32) */
   int64_t step;        /* steps taken (t) */
   uint64_t device_bytes; /* device memory held by the handle */
+  uint64_t select_fallbacks; /* chunks (over all steps) whose top-k the standalone select
+                                redid because their threshold bucket held too many ties */
 } scape_info_t;
 
 /* Create a handle: computes the chunk/shard table, allocates all state on the
@@ -124,7 +124,7 @@ int scape_mask(scape_handle* h, uint32_t* out_bits);
 /* Free everything the handle owns (waits for its last step). NULL is a no-op. */
 void scape_destroy(scape_handle* h);
 
-/* Sizes and counters of the handle. */
+/* Sizes and counters of the handle (waits for the last step). */
 int scape_info(const scape_handle* h, scape_info_t* out);
 
 /* Copy elements [offset, offset+count) of a state field (worker w for U and

@@ -1,0 +1,483 @@
+// The SCAPE step, one chunk at a time, in one persistent kernel.
+//
+// SCAPE (arXiv 2607.01678; gist.science technical summary §2) aligns mask
+// generation with optimizer sharding: worker w builds the top-k mask only for
+// the chunks of its own shard, from its first-moment accumulator, and the mask
+// is applied one step later.  Here the chunk is the unit of work: a CTA takes
+// chunk c (C coordinates, owner w_c = c / q) and runs every step of the rule on
+// it before moving to the next chunk, so each state array is streamed through
+// HBM exactly once per step and the selection runs on-chip.
+//
+// Phases per chunk (1024 threads, ~180 KB of shared memory, one CTA per SM):
+//  0. load the chunk's words of M_{t-1} and their exclusive popcount prefix:
+//     the packed position of a kept coordinate i is
+//       base_c + popcount(M_{t-1} bits of the chunk before i),
+//     base_c = c * k_full (every earlier chunk keeps exactly k coordinates);
+//  1. the owner's streaming pass (momentum, accumulate, mask select, residual,
+//     compaction into vals_owner), which also keeps every |a| as a 16-bit
+//     truncated key (fp32 bits 30..15) in shared memory and counts its top 12
+//     bits in a 4096-bin histogram;
+//  2. exact top-k_c of the owner's |a| with ties to the lower index: the
+//     histogram gives the 12-bit bin of the k-th largest, a 16-bin pass over
+//     the stored keys its 16-bit bucket; every key above that bucket is kept,
+//     every key below dropped, and the coordinates inside it (usually a few
+//     hundred) get their full 31-bit keys back from what phase 1 wrote (vals
+//     on the applied mask, else the new residual) and are ranked on the
+//     unique composite (key << 16 | 0xFFFF - index).  The chunk's mask words
+//     are assembled in shared memory and stored.  A bucket with more than
+//     kCap coordinates (massive ties) flags the chunk; the standalone radix
+//     select redoes such chunks after this kernel;
+//  3. the streaming pass of every other worker;
+//  4. the "all-reduce": bbar = (vals_0 + ... + vals_{W-1}) * (1/W) for the
+//     chunk's kept coordinates, read back from the compact buffers the
+//     workers wrote (the only place worker data meets), then v and theta for
+//     every coordinate of the chunk.
+// Arithmetic is the fp32 rule of the library header, with the same
+// parenthesisation and no FMA contraction (built with -fmad=false).
+//
+// Per coordinate the HBM traffic is W*(2 g + 8 u + 8 e + 1/8 mask) + 8 theta +
+// 8 v + 1/8 new mask bytes, plus 4 B per kept value per worker written and
+// read back and 8 B per kept coordinate (bbar, idx) -- the compulsory bytes.
+#include "scape_device.cuh"
+#include "scape_kernels.cuh"
+
+namespace scape {
+namespace {
+
+constexpr int kNT = 1024;
+constexpr int kNW = kNT / 32;
+constexpr uint32_t kCap = 2048;          // candidates ranked in shared memory
+constexpr uint32_t kRankCountMax = 1024; // up to this many: direct rank count
+constexpr int kTB = 47;                  // composite key bits
+
+// dynamic shared memory layout (bytes)
+constexpr uint32_t kOffKey16 = 0;                      // uint16[65536]
+constexpr uint32_t kOffHist = kOffKey16 + 65536 * 2;   // uint32[4096]
+constexpr uint32_t kOffWprev = kOffHist + 4096 * 4;    // uint32[2048]
+constexpr uint32_t kOffMword = kOffWprev + 2048 * 4;   // uint32[2048]
+constexpr uint32_t kOffWpre = kOffMword + 2048 * 4;    // uint16[2048]
+constexpr uint32_t kOffCand = kOffWpre + 2048 * 2;     // uint64[kCap]
+constexpr uint32_t kOffScan = kOffCand + kCap * 8;     // uint32[64]
+constexpr uint32_t kOffCtl = kOffScan + 64 * 4;        // uint32[32]
+constexpr uint32_t kSmemBytes = kOffCtl + 32 * 4;
+
+// ctl[] slots
+enum { C_BIN = 0, C_ABOVE = 1, C_CNT = 2, C_NCAND = 3, C_SUB = 8 /* 16 entries */ };
+
+struct Shared {
+  uint16_t* key16;
+  uint32_t* hist;
+  uint32_t* wprev;
+  uint32_t* mword;
+  uint16_t* wpre;
+  unsigned long long* cand;
+  uint32_t* scan;
+  uint32_t* ctl;
+};
+
+__device__ __forceinline__ Shared carve(unsigned char* s) {
+  Shared sh;
+  sh.key16 = reinterpret_cast<uint16_t*>(s + kOffKey16);
+  sh.hist = reinterpret_cast<uint32_t*>(s + kOffHist);
+  sh.wprev = reinterpret_cast<uint32_t*>(s + kOffWprev);
+  sh.mword = reinterpret_cast<uint32_t*>(s + kOffMword);
+  sh.wpre = reinterpret_cast<uint16_t*>(s + kOffWpre);
+  sh.cand = reinterpret_cast<unsigned long long*>(s + kOffCand);
+  sh.scan = reinterpret_cast<uint32_t*>(s + kOffScan);
+  sh.ctl = reinterpret_cast<uint32_t*>(s + kOffCtl);
+  return sh;
+}
+
+struct Chunk {
+  uint64_t c, c0, base;  // index, first coordinate, first packed position
+  uint32_t L, k, nw;     // length, kept count, mask words
+  int owner;
+};
+
+// Phases 1 and 3: worker w's streaming pass over the chunk.  One warp per
+// 256-coordinate tile, 8 consecutive coordinates per thread (16-byte loads).
+template <bool OWNER>
+__device__ __forceinline__ void stream_worker(const FusedArgs& p, const Shared& sh,
+                                              const Chunk& ch, int w) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint16_t* __restrict__ g = p.grads[w] + ch.c0;
+  float* __restrict__ u = p.u + (uint64_t)w * p.Np + ch.c0;
+  float* __restrict__ e = p.e + (uint64_t)w * p.Np + ch.c0;
+  float* __restrict__ vals = p.vals + (uint64_t)w * p.Kp + ch.base;
+  const float b1 = p.b1, c1 = p.c1;
+  const uint32_t ntile = (ch.L + 255) / 256;
+  for (uint32_t t = warp; t < ntile; t += kNW) {
+    const uint32_t i0 = t * 256 + lane * 8;
+    if (i0 >= ch.L) continue;
+    const uint32_t j = i0 >> 5;
+    const uint32_t word = sh.wprev[j];
+    const uint32_t sft = (lane & 3) * 8;
+    const uint32_t byte = (word >> sft) & 0xFFu;
+    const uint32_t rank0 = sh.wpre[j] + __popc(word & ((1u << sft) - 1u));
+    if (i0 + 8 <= ch.L) {
+      const uint4 gr = ld_stream_u4(g + i0);
+      float4* up = reinterpret_cast<float4*>(u + i0);
+      float4* ep = reinterpret_cast<float4*>(e + i0);
+      const float4 u0 = up[0], u1 = up[1], e0 = ep[0], e1 = ep[1];
+      float gf[8] = {bf16lo(gr.x), bf16hi(gr.x), bf16lo(gr.y), bf16hi(gr.y),
+                     bf16lo(gr.z), bf16hi(gr.z), bf16lo(gr.w), bf16hi(gr.w)};
+      float uu[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+      float ee[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
+      uint32_t k16[8];
+#pragma unroll
+      for (int jj = 0; jj < 8; jj++) {
+        const float un = (b1 * uu[jj]) + (c1 * gf[jj]);
+        const float a = ee[jj] + un;
+        const bool m = (byte >> jj) & 1u;
+        const float b = m ? a : 0.0f;
+        uu[jj] = un;
+        ee[jj] = a - b;
+        if (m) vals[rank0 + __popc(byte & ((1u << jj) - 1u))] = b;
+        if (OWNER) {
+          const uint32_t key = __float_as_uint(a) & 0x7FFFFFFFu;
+          k16[jj] = key >> 15;
+          atomicAdd(&sh.hist[key >> 19], 1u);
+        }
+      }
+      up[0] = make_float4(uu[0], uu[1], uu[2], uu[3]);
+      up[1] = make_float4(uu[4], uu[5], uu[6], uu[7]);
+      ep[0] = make_float4(ee[0], ee[1], ee[2], ee[3]);
+      ep[1] = make_float4(ee[4], ee[5], ee[6], ee[7]);
+      if (OWNER) {
+        uint4 kv;
+        kv.x = k16[0] | (k16[1] << 16);
+        kv.y = k16[2] | (k16[3] << 16);
+        kv.z = k16[4] | (k16[5] << 16);
+        kv.w = k16[6] | (k16[7] << 16);
+        *reinterpret_cast<uint4*>(sh.key16 + i0) = kv;
+      }
+    } else {
+      const uint32_t nv = ch.L - i0;
+      for (uint32_t jj = 0; jj < nv; jj++) {
+        const float un = (b1 * u[i0 + jj]) + (c1 * bf16f(g[i0 + jj]));
+        const float a = e[i0 + jj] + un;
+        const bool m = (byte >> jj) & 1u;
+        const float b = m ? a : 0.0f;
+        u[i0 + jj] = un;
+        e[i0 + jj] = a - b;
+        if (m) vals[rank0 + __popc(byte & ((1u << jj) - 1u))] = b;
+        if (OWNER) {
+          const uint32_t key = __float_as_uint(a) & 0x7FFFFFFFu;
+          sh.key16[i0 + jj] = (uint16_t)(key >> 15);
+          atomicAdd(&sh.hist[key >> 19], 1u);
+        }
+      }
+    }
+  }
+}
+
+// Full 31-bit key of the owner's accumulator at chunk coordinate i, rebuilt
+// from what phase 1 wrote: the kept value on M_{t-1}, else the residual.
+__device__ __forceinline__ uint32_t owner_key(const FusedArgs& p, const Shared& sh,
+                                              const Chunk& ch, uint32_t i) {
+  const uint32_t j = i >> 5, bit = i & 31;
+  const uint32_t word = sh.wprev[j];
+  float a;
+  if ((word >> bit) & 1u) {
+    const uint32_t r = sh.wpre[j] + __popc(word & ((1u << bit) - 1u));
+    a = p.vals[(uint64_t)ch.owner * p.Kp + ch.base + r];
+  } else {
+    a = p.e[(uint64_t)ch.owner * p.Np + ch.c0 + i];
+  }
+  return __float_as_uint(a) & 0x7FFFFFFFu;
+}
+
+// Phase 2.  Leaves the chunk's mask words in sh.mword; returns false when the
+// chunk must be redone by the standalone select (too many tied candidates).
+__device__ bool select_chunk(const FusedArgs& p, const Shared& sh, const Chunk& ch) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  const uint32_t L = ch.L, k = ch.k;
+  uint32_t T16 = 0;     // keys above this 16-bit bucket are kept
+  bool take_bucket;     // keep the whole bucket T16 too
+  bool ranked = false;  // bucket T16 resolved through candidates
+  uint32_t r2 = 0, ncand = 0;
+
+  if (k == 0 || k == L) {
+    for (uint32_t j = tid; j < ch.nw; j += kNT) {
+      uint32_t word = 0u;
+      if (k != 0) word = (j == ch.nw - 1 && (L & 31)) ? ((1u << (L & 31)) - 1u) : 0xFFFFFFFFu;
+      sh.mword[j] = word;
+    }
+    __syncthreads();
+    return true;
+  }
+  find_bin<kNT>(sh.hist, 4096, k, sh.scan, sh.ctl);
+  const uint32_t b12 = sh.ctl[C_BIN], cnt12 = sh.ctl[C_CNT];
+  const uint32_t r1 = k - sh.ctl[C_ABOVE];
+  if (r1 == cnt12) {
+    T16 = b12 << 4;
+    take_bucket = true;
+  } else {
+    // 16 sub-buckets of the threshold bin
+    if (tid < 16) sh.ctl[C_SUB + tid] = 0;
+    __syncthreads();
+    for (uint32_t i = tid; i < L; i += kNT) {
+      const uint32_t k16 = sh.key16[i];
+      if ((k16 >> 4) == b12) atomicAdd(&sh.ctl[C_SUB + (k16 & 15u)], 1u);
+    }
+    __syncthreads();
+    if (tid == 0) {
+      uint32_t acc = 0;
+      for (int b = 15; b >= 0; b--) {
+        const uint32_t h = sh.ctl[C_SUB + b];
+        if (acc + h >= r1) {
+          sh.ctl[C_BIN] = (b12 << 4) | (uint32_t)b;
+          sh.ctl[C_ABOVE] = r1 - acc;
+          sh.ctl[C_CNT] = h;
+          break;
+        }
+        acc += h;
+      }
+      sh.ctl[C_NCAND] = 0;
+    }
+    __syncthreads();
+    T16 = sh.ctl[C_BIN];
+    r2 = sh.ctl[C_ABOVE];
+    const uint32_t cnt16 = sh.ctl[C_CNT];
+    take_bucket = (r2 == cnt16);
+    if (!take_bucket) {
+      if (cnt16 > kCap) return false;  // uniform: every thread read the same cnt16
+      ranked = true;
+      // candidates: coordinates in bucket T16, with their full composite key
+      for (uint32_t base = (tid & ~31u); base < L; base += kNT) {
+        const uint32_t i = base + lane;
+        const bool is = i < L && sh.key16[i] == T16;
+        const unsigned bal = __ballot_sync(kFull, is);
+        uint32_t pos = 0;
+        if (lane == 0 && bal) pos = atomicAdd(&sh.ctl[C_NCAND], __popc(bal));
+        pos = __shfl_sync(kFull, pos, 0);
+        if (is) {
+          const uint32_t key = owner_key(p, sh, ch, i);
+          sh.cand[pos + __popc(bal & ((1u << lane) - 1u))] =
+              ((unsigned long long)key << 16) | (unsigned long long)(0xFFFFu - i);
+        }
+      }
+      __syncthreads();
+      ncand = sh.ctl[C_NCAND];
+    }
+  }
+
+  // mask words from the stored keys
+  for (uint32_t j = tid; j < ch.nw; j += kNT) {
+    uint32_t word = 0u;
+    const uint32_t i0 = j * 32;
+    if (i0 + 32 <= L) {
+      const uint4* kp = reinterpret_cast<const uint4*>(sh.key16 + i0);
+#pragma unroll
+      for (int q = 0; q < 4; q++) {
+        const uint4 v = kp[q];
+        const uint32_t h[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int s = 0; s < 4; s++) {
+          const uint32_t lo = h[s] & 0xFFFFu, hi = h[s] >> 16;
+          const uint32_t bit = q * 8 + s * 2;
+          if (lo > T16 || (take_bucket && lo == T16)) word |= 1u << bit;
+          if (hi > T16 || (take_bucket && hi == T16)) word |= 1u << (bit + 1);
+        }
+      }
+    } else {
+      for (uint32_t b = 0; b < 32 && i0 + b < L; b++) {
+        const uint32_t k16 = sh.key16[i0 + b];
+        if (k16 > T16 || (take_bucket && k16 == T16)) word |= 1u << b;
+      }
+    }
+    sh.mword[j] = word;
+  }
+  __syncthreads();
+
+  if (ranked) {
+    if (ncand <= kRankCountMax) {
+      // direct rank: keep candidate m iff fewer than r2 candidates are larger
+      for (uint32_t m = tid; m < ncand; m += kNT) {
+        const unsigned long long X = sh.cand[m];
+        uint32_t above = 0;
+        for (uint32_t o = 0; o < ncand; o++) above += sh.cand[o] > X;
+        if (above < r2) {
+          const uint32_t i = 0xFFFFu - (uint32_t)(X & 0xFFFFu);
+          atomicOr(&sh.mword[i >> 5], 1u << (i & 31));
+        }
+      }
+    } else {
+      // radix over the low 31 bits (all candidates share the top 16 = T16)
+      unsigned long long pf = T16;
+      int pb = 16;
+      uint32_t rr = r2;
+      while (true) {
+        const int d = (kTB - pb) < 12 ? (kTB - pb) : 12;
+        const int nb = 1 << d;
+        const int shift = kTB - pb - d;
+        for (int i = tid; i < nb; i += kNT) sh.hist[i] = 0;
+        __syncthreads();
+        for (uint32_t m = tid; m < ncand; m += kNT) {
+          const unsigned long long X = sh.cand[m];
+          if ((X >> (kTB - pb)) == pf)
+            atomicAdd(&sh.hist[(uint32_t)(X >> shift) & (uint32_t)(nb - 1)], 1u);
+        }
+        __syncthreads();
+        find_bin<kNT>(sh.hist, nb, rr, sh.scan, sh.ctl);
+        const uint32_t b = sh.ctl[C_BIN], above = sh.ctl[C_ABOVE], cnt = sh.ctl[C_CNT];
+        __syncthreads();
+        rr -= above;
+        pf = (pf << d) | b;
+        pb += d;
+        if (rr == cnt) break;
+      }
+      const unsigned long long T = pf << (kTB - pb);
+      for (uint32_t m = tid; m < ncand; m += kNT) {
+        const unsigned long long X = sh.cand[m];
+        if (X >= T) {
+          const uint32_t i = 0xFFFFu - (uint32_t)(X & 0xFFFFu);
+          atomicOr(&sh.mword[i >> 5], 1u << (i & 31));
+        }
+      }
+    }
+    __syncthreads();
+  }
+  return true;
+}
+
+// Phase 4: fixed-order W-way sum of the compact buffers and the AdamS update.
+__device__ __forceinline__ void update_chunk(const FusedArgs& p, const Shared& sh,
+                                             const Chunk& ch) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  float* __restrict__ th = p.theta + ch.c0;
+  float* __restrict__ vv = p.v + ch.c0;
+  const float b2 = p.b2, c2 = p.c2, lr = p.lr, wd = p.wd, eps = p.eps, invW = p.invW;
+  const uint32_t ntile = (ch.L + 255) / 256;
+  for (uint32_t t = warp; t < ntile; t += kNW) {
+    const uint32_t i0 = t * 256 + lane * 8;
+    if (i0 >= ch.L) continue;
+    const uint32_t j = i0 >> 5;
+    const uint32_t word = sh.wprev[j];
+    const uint32_t sft = (lane & 3) * 8;
+    const uint32_t byte = (word >> sft) & 0xFFu;
+    const uint32_t rank0 = (uint32_t)ch.base + sh.wpre[j] + __popc(word & ((1u << sft) - 1u));
+    const uint32_t nv = (ch.L - i0) < 8 ? (ch.L - i0) : 8;
+    float tt[8], vo[8];
+    if (nv == 8) {
+      const float4 t0 = reinterpret_cast<const float4*>(th + i0)[0];
+      const float4 t1 = reinterpret_cast<const float4*>(th + i0)[1];
+      const float4 v0 = reinterpret_cast<const float4*>(vv + i0)[0];
+      const float4 v1 = reinterpret_cast<const float4*>(vv + i0)[1];
+      tt[0] = t0.x; tt[1] = t0.y; tt[2] = t0.z; tt[3] = t0.w;
+      tt[4] = t1.x; tt[5] = t1.y; tt[6] = t1.z; tt[7] = t1.w;
+      vo[0] = v0.x; vo[1] = v0.y; vo[2] = v0.z; vo[3] = v0.w;
+      vo[4] = v1.x; vo[5] = v1.y; vo[6] = v1.z; vo[7] = v1.w;
+    } else {
+      for (uint32_t jj = 0; jj < 8; jj++) {
+        tt[jj] = jj < nv ? th[i0 + jj] : 0.0f;
+        vo[jj] = jj < nv ? vv[i0 + jj] : 0.0f;
+      }
+    }
+#pragma unroll
+    for (int jj = 0; jj < 8; jj++) {
+      const bool m = (byte >> jj) & 1u;
+      float bb = 0.0f;
+      if (m) {
+        const uint32_t r = rank0 + __popc(byte & ((1u << jj) - 1u));
+        float s = p.vals[r];
+        for (int w = 1; w < p.W; w++) s = s + p.vals[(uint64_t)w * p.Kp + r];
+        bb = s * invW;
+        p.bbar[r] = bb;
+        p.idx[r] = (uint32_t)(ch.c0 + i0 + jj);
+      }
+      const float vn = (b2 * vo[jj]) + (c2 * (bb * bb));
+      const float q = m ? bb / (sqrtf(vn) + eps) : 0.0f;
+      vo[jj] = vn;
+      tt[jj] = tt[jj] - (lr * (q + (wd * tt[jj])));
+    }
+    if (nv == 8) {
+      reinterpret_cast<float4*>(th + i0)[0] = make_float4(tt[0], tt[1], tt[2], tt[3]);
+      reinterpret_cast<float4*>(th + i0)[1] = make_float4(tt[4], tt[5], tt[6], tt[7]);
+      reinterpret_cast<float4*>(vv + i0)[0] = make_float4(vo[0], vo[1], vo[2], vo[3]);
+      reinterpret_cast<float4*>(vv + i0)[1] = make_float4(vo[4], vo[5], vo[6], vo[7]);
+    } else {
+      for (uint32_t jj = 0; jj < nv; jj++) {
+        th[i0 + jj] = tt[jj];
+        vv[i0 + jj] = vo[jj];
+      }
+    }
+  }
+}
+
+__global__ __launch_bounds__(kNT, 1) void step_chunks(const FusedArgs p) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  const Shared sh = carve(smem_raw);
+  const int tid = threadIdx.x;
+
+  for (uint64_t c = blockIdx.x; c < p.n_ch; c += gridDim.x) {
+    Chunk ch;
+    ch.c = c;
+    ch.c0 = c * p.C;
+    ch.L = (uint32_t)((p.N - ch.c0) < p.C ? (p.N - ch.c0) : p.C);
+    ch.k = (c == p.n_ch - 1) ? p.k_last : p.k_full;
+    ch.nw = (ch.L + 31) / 32;
+    ch.base = c * (uint64_t)p.k_full;
+    ch.owner = (int)(c / p.q);
+
+    // phase 0: M_{t-1} words of the chunk, their popcount prefix; clear the histogram
+    {
+      const uint32_t* mp = p.mprev + ch.c0 / 32;
+      const uint32_t j0 = tid * 2;
+      const uint32_t w0 = j0 < ch.nw ? mp[j0] : 0u;
+      const uint32_t w1 = j0 + 1 < ch.nw ? mp[j0 + 1] : 0u;
+      const uint32_t cnt = __popc(w0) + __popc(w1);
+      uint32_t total;
+      const uint32_t inc = block_incl_scan<kNT>(cnt, sh.scan, &total);
+      if (j0 < 2048) {
+        sh.wprev[j0] = w0;
+        sh.wprev[j0 + 1] = w1;
+        sh.wpre[j0] = (uint16_t)(inc - cnt);
+        sh.wpre[j0 + 1] = (uint16_t)(inc - cnt + __popc(w0));
+      }
+      for (int i = tid; i < 4096; i += kNT) sh.hist[i] = 0;
+      __syncthreads();
+    }
+
+    // phase 1: the owner's pass, keeping its keys
+    stream_worker<true>(p, sh, ch, ch.owner);
+    __syncthreads();
+
+    // phase 2: top-k of the owner's |a| -> mask words of M_t
+    const bool ok = select_chunk(p, sh, ch);
+    if (ok) {
+      uint32_t* mo = p.mout + ch.c0 / 32;
+      for (uint32_t j = tid; j < ch.nw; j += kNT) mo[j] = sh.mword[j];
+    } else if (tid == 0) {
+      p.fallback[c] = 1u;
+      atomicAdd(p.n_fallback, 1u);
+    }
+
+    // phase 3: every other worker
+    for (int w = 0; w < p.W; w++)
+      if (w != ch.owner) stream_worker<false>(p, sh, ch, w);
+    __syncthreads();
+
+    // phase 4: synchronized buffer, second moment, parameters
+    update_chunk(p, sh, ch);
+    __syncthreads();
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_step_chunks(const FusedArgs& a, cudaStream_t s) {
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(step_chunks, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  uint64_t grid = (uint64_t)num_sms();
+  if (grid > a.n_ch) grid = a.n_ch;
+  step_chunks<<<(unsigned)grid, kNT, kSmemBytes, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace scape

@@ -1,4 +1,10 @@
-// Kernel (c): partitioned mask generation of SCAPE, M_t.
+// Standalone partitioned mask generation of SCAPE (radix select).
+//
+// Used for the step-0 mask M_{-1} (every chunk, from the step-0 accumulators)
+// and, after the fused step kernel, for the few chunks whose 16-bit threshold
+// bucket held more tied coordinates than its shared-memory candidate list
+// (those chunks are flagged; this kernel redoes exactly them and clears the
+// flags).  One CTA per chunk at a time, grid-strided over the chunks.
 //
 // SCAPE builds the mask from first-moment statistics, each worker only over
 // its own optimizer shard, and the shard masks together form the global mask
@@ -124,10 +130,8 @@ __device__ __forceinline__ int quad_keys(const SelectArgs& p, const SelectSmem& 
 }
 
 template <int SRC>
-__global__ __launch_bounds__(kNT, 2) void select_topk(const SelectArgs p) {
-  __shared__ SelectSmem sm;
+__device__ void select_one(const SelectArgs& p, SelectSmem& sm, const uint64_t c) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const uint64_t c = blockIdx.x;
   const uint64_t c0 = c * p.C;
   const uint32_t L = (uint32_t)((p.N - c0) < p.C ? (p.N - c0) : p.C);
   const uint32_t k = (c == p.n_ch - 1) ? p.k_last : p.k_full;
@@ -277,13 +281,26 @@ __global__ __launch_bounds__(kNT, 2) void select_topk(const SelectArgs p) {
   }
 }
 
+template <int SRC>
+__global__ __launch_bounds__(kNT, 2) void select_topk(const SelectArgs p) {
+  __shared__ SelectSmem sm;
+  for (uint64_t c = blockIdx.x; c < p.n_ch; c += gridDim.x) {
+    if (p.flags && p.flags[c] == 0u) continue;
+    select_one<SRC>(p, sm, c);
+    __syncthreads();
+    if (p.flags && threadIdx.x == 0) p.flags[c] = 0u;
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_select(const SelectArgs& a, bool boot, cudaStream_t s) {
+  uint64_t grid = (uint64_t)num_sms() * 2;
+  if (grid > a.n_ch) grid = a.n_ch;
   if (boot)
-    select_topk<SRC_BOOT><<<(unsigned)a.n_ch, kNT, 0, s>>>(a);
+    select_topk<SRC_BOOT><<<(unsigned)grid, kNT, 0, s>>>(a);
   else
-    select_topk<SRC_STATE><<<(unsigned)a.n_ch, kNT, 0, s>>>(a);
+    select_topk<SRC_STATE><<<(unsigned)grid, kNT, 0, s>>>(a);
   return cudaGetLastError();
 }
 

@@ -31,7 +31,7 @@ using namespace scape;
 
 struct scape_handle {
   // geometry
-  uint64_t N = 0, Np = 0, n_wt = 0, n_blk = 0, mask_words = 0, mask_alloc = 0;
+  uint64_t N = 0, Np = 0, mask_words = 0, mask_alloc = 0;
   uint32_t C = 0;
   int W = 0;
   double density = 0;
@@ -44,7 +44,8 @@ struct scape_handle {
   float *vals = nullptr, *bbar = nullptr;
   uint32_t* idx = nullptr;
   uint32_t* mask[2] = {nullptr, nullptr};
-  uint32_t *toff_local = nullptr, *bsum = nullptr;
+  uint32_t* fallback = nullptr;    // per chunk, see k_fused.cu
+  uint32_t* n_fallback = nullptr;  // chunks redone by the standalone select (running total)
   uint16_t* stage = nullptr;  // scape_step_host staging, W x N bf16
   int prev = 0;               // mask[prev] = M_{t-1} for the next step
   bool has_mask = false;      // a mask exists (built by a step or loaded)
@@ -90,7 +91,7 @@ cudaError_t dalloc(scape_handle* h, T** p, uint64_t count) {
 
 void release(scape_handle* h) {
   void* ps[] = {h->theta, h->v, h->u, h->e, h->vals, h->bbar, h->idx, h->mask[0], h->mask[1],
-                h->toff_local, h->bsum, h->stage};
+                h->fallback, h->n_fallback, h->stage};
   for (void* p : ps)
     if (p) cudaFree(p);
   for (cudaEvent_t ev : h->ev_pool) cudaEventDestroy(ev);
@@ -202,10 +203,8 @@ SCAPE_API int scape_create(const scape_layout* layout, int W, double density, fl
   h->c2 = 1.0f - beta2;
   h->invW = 1.0f / (float)W;
   h->Np = (N + kTile - 1) / kTile * kTile;
-  h->n_wt = h->Np / kTile;
-  h->n_blk = (h->n_wt + kTilesPerBlk - 1) / kTilesPerBlk;
   h->mask_words = (N + 31) / 32;
-  h->mask_alloc = h->n_wt * 8;
+  h->mask_alloc = h->Np / 32;
   h->n_ch = (N + C - 1) / C;
   h->q = (h->n_ch + W - 1) / W;
   h->k_full = (uint32_t)std::floor(density * (double)C);
@@ -224,8 +223,8 @@ SCAPE_API int scape_create(const scape_layout* layout, int W, double density, fl
   if (e == cudaSuccess) e = dalloc(h, &h->idx, h->Kp);
   if (e == cudaSuccess) e = dalloc(h, &h->mask[0], h->mask_alloc);
   if (e == cudaSuccess) e = dalloc(h, &h->mask[1], h->mask_alloc);
-  if (e == cudaSuccess) e = dalloc(h, &h->toff_local, h->n_wt);
-  if (e == cudaSuccess) e = dalloc(h, &h->bsum, h->n_blk);
+  if (e == cudaSuccess) e = dalloc(h, &h->fallback, h->n_ch);
+  if (e == cudaSuccess) e = dalloc(h, &h->n_fallback, 1);
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {
     const int code = (e == cudaErrorMemoryAllocation) ? SCAPE_ENOMEM : SCAPE_ECUDA;
@@ -264,6 +263,12 @@ SCAPE_API int scape_info(const scape_handle* h, scape_info_t* out) {
   out->mask_words = h->mask_words;
   out->step = h->t;
   out->device_bytes = h->device_bytes;
+  uint32_t nf = 0;
+  scape_handle* hm = const_cast<scape_handle*>(h);
+  if (wait_last(hm) != cudaSuccess ||
+      cudaMemcpy(&nf, h->n_fallback, 4, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return cuda_fail(hm, cudaGetLastError(), "scape_info");
+  out->select_fallbacks = nf;
   return SCAPE_OK;
 }
 
@@ -292,64 +297,51 @@ static int step_device(scape_handle* h, const uint16_t* const* g, cudaStream_t s
     PhaseTimer pt(h, SCAPE_PH_SELECT_BOOT, s);
     sa.mprev = nullptr;
     sa.mout = mprev;
+    sa.flags = nullptr;
     if ((e = launch_select(sa, true, s)) != cudaSuccess) return cuda_fail(h, e, "select (step 0)");
     pt.done();
   }
   {
-    PhaseTimer pt(h, SCAPE_PH_OFFSETS, s);
-    if ((e = launch_offsets(mprev, h->toff_local, h->bsum, h->n_wt, s)) != cudaSuccess)
-      return cuda_fail(h, e, "offsets");
-    pt.done();
-  }
-  {
-    StreamArgs a{};
+    FusedArgs a{};
     for (int w = 0; w < h->W; w++) a.grads[w] = g[w];
     a.u = h->u;
     a.e = h->e;
     a.vals = h->vals;
-    a.mprev = mprev;
-    a.toff_local = h->toff_local;
-    a.bsum = h->bsum;
-    a.N = h->N;
-    a.Np = h->Np;
-    a.Kp = h->Kp;
-    a.n_wt = h->n_wt;
-    a.b1 = h->b1;
-    a.c1 = h->c1;
-    PhaseTimer pt(h, SCAPE_PH_STREAM, s);
-    if ((e = launch_stream_compact(a, h->W, s)) != cudaSuccess)
-      return cuda_fail(h, e, "stream_compact");
-    pt.done();
-  }
-  {
-    UpdateArgs a{};
     a.theta = h->theta;
     a.v = h->v;
-    a.vals = h->vals;
     a.bbar = h->bbar;
     a.idx = h->idx;
     a.mprev = mprev;
-    a.toff_local = h->toff_local;
-    a.bsum = h->bsum;
+    a.mout = mcur;
+    a.fallback = h->fallback;
+    a.n_fallback = h->n_fallback;
     a.N = h->N;
+    a.Np = h->Np;
     a.Kp = h->Kp;
-    a.n_wt = h->n_wt;
+    a.n_ch = h->n_ch;
+    a.q = h->q;
+    a.C = h->C;
+    a.k_full = h->k_full;
+    a.k_last = h->k_last;
     a.W = h->W;
+    a.b1 = h->b1;
+    a.c1 = h->c1;
     a.b2 = h->b2;
     a.c2 = h->c2;
     a.lr = h->lr;
     a.wd = h->wd;
     a.eps = h->eps;
     a.invW = h->invW;
-    PhaseTimer pt(h, SCAPE_PH_UPDATE, s);
-    if ((e = launch_reduce_update(a, s)) != cudaSuccess) return cuda_fail(h, e, "reduce_update");
+    PhaseTimer pt(h, SCAPE_PH_STEP, s);
+    if ((e = launch_step_chunks(a, s)) != cudaSuccess) return cuda_fail(h, e, "step kernel");
     pt.done();
   }
-  {
+  {  // chunks whose threshold bucket overflowed the on-chip candidate list
     sa.mprev = mprev;
     sa.mout = mcur;
-    PhaseTimer pt(h, SCAPE_PH_SELECT, s);
-    if ((e = launch_select(sa, false, s)) != cudaSuccess) return cuda_fail(h, e, "select");
+    sa.flags = h->fallback;
+    PhaseTimer pt(h, SCAPE_PH_SELECT_FALLBACK, s);
+    if ((e = launch_select(sa, false, s)) != cudaSuccess) return cuda_fail(h, e, "select (fallback)");
     pt.done();
   }
   h->prev = 1 - h->prev;

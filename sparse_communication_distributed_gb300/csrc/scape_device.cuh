@@ -40,6 +40,37 @@ __device__ __forceinline__ uint32_t block_incl_scan(uint32_t x, uint32_t* warp_t
   return r;
 }
 
+// Finds, in hist[0..nb) (nb a power of two), the bin holding the r-th largest
+// element (1-based, r <= total): out[0] = bin, out[1] = count in the bins above
+// it, out[2] = its count.  Block-wide (NT threads); ends with __syncthreads().
+template <int NT>
+__device__ void find_bin(const uint32_t* hist, int nb, uint32_t r, uint32_t* scan,
+                         uint32_t* out) {
+  const int t = threadIdx.x;
+  const int bpt = nb >= NT ? nb / NT : 1;
+  const int b0 = t * bpt;
+  uint32_t s = 0;
+  if (b0 < nb)
+    for (int j = 0; j < bpt; j++) s += hist[b0 + j];
+  uint32_t total;
+  const uint32_t inc = block_incl_scan<NT>(s, scan, &total);
+  const uint32_t above = total - inc;
+  if (b0 < nb && above < r && r <= above + s) {
+    uint32_t acc = above;
+    for (int j = bpt - 1; j >= 0; j--) {
+      const uint32_t h = hist[b0 + j];
+      if (acc + h >= r) {
+        out[0] = (uint32_t)(b0 + j);
+        out[1] = acc;
+        out[2] = h;
+        break;
+      }
+      acc += h;
+    }
+  }
+  __syncthreads();
+}
+
 __device__ __forceinline__ float bf16lo(uint32_t x) { return __uint_as_float(x << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t x) { return __uint_as_float(x & 0xFFFF0000u); }
 __device__ __forceinline__ float bf16f(uint16_t h) { return __uint_as_float((uint32_t)h << 16); }

@@ -3,15 +3,13 @@
 // Data layout in HBM (all allocations by the library):
 //   theta, v      fp32[Np]            Np = N rounded up to 256
 //   u, e          fp32[W][Np]
-//   mask[2]       uint32[n_wt*8]      M_{t-1} / M_t, bit j of word i = coord 32i+j
+//   mask[2]       uint32[Np/32]       M_{t-1} / M_t, bit j of word i = coord 32i+j
 //   vals          fp32[W][Kp]         compact b_w, ascending coordinate
 //   bbar          fp32[Kp]            compact synchronized buffer
 //   idx           uint32[Kp]          coordinates of the compact entries
-//   toff_local    uint32[n_wt]        kept-count before each 256-coordinate tile,
-//                                     counted from its 65536-coordinate block
-//   bsum          uint32[n_blk]       kept-count before each block (after the scan)
-// A "tile" is 256 consecutive coordinates = 8 mask words = one warp of 32
-// threads x 8 coordinates; blocks are 256 tiles.
+//   fallback      uint32[n_ch]        chunks whose selection the standalone select redoes
+// Chunk c (C coordinates, the last one ragged) keeps exactly k_c coordinates,
+// so its kept values start at packed position c * k_full.
 #pragma once
 #include <cstdint>
 #include <cuda_runtime.h>
@@ -19,34 +17,26 @@
 namespace scape {
 
 constexpr int kMaxW = 64;
-constexpr int kTile = 256;             // coordinates per warp tile
-constexpr int kTilesPerBlk = 256;      // warp tiles per offsets block
+constexpr int kTile = 256;             // coordinates per warp tile (8 per thread)
 constexpr uint32_t kMaxChunk = 65536;  // largest chunk (16-bit in-chunk index)
 
-struct StreamArgs {
+struct FusedArgs {
   const uint16_t* grads[kMaxW];
   float* u;
   float* e;
   float* vals;
-  const uint32_t* mprev;
-  const uint32_t* toff_local;
-  const uint32_t* bsum;
-  uint64_t N, Np, Kp, n_wt;
-  float b1, c1;
-};
-
-struct UpdateArgs {
   float* theta;
   float* v;
-  const float* vals;
   float* bbar;
   uint32_t* idx;
   const uint32_t* mprev;
-  const uint32_t* toff_local;
-  const uint32_t* bsum;
-  uint64_t N, Kp, n_wt;
+  uint32_t* mout;
+  uint32_t* fallback;    // per chunk: 1 = selection left to the standalone select
+  uint32_t* n_fallback;  // count of such chunks (diagnostic)
+  uint64_t N, Np, Kp, n_ch, q;
+  uint32_t C, k_full, k_last;
   int W;
-  float b2, c2, lr, wd, eps, invW;
+  float b1, c1, b2, c2, lr, wd, eps, invW;
 };
 
 struct SelectArgs {
@@ -59,15 +49,13 @@ struct SelectArgs {
   const float* u;
   float b1, c1;
   uint32_t* mout;
+  uint32_t* flags;  // NULL: every chunk; else only chunks with flags[c] != 0 (cleared)
   uint64_t N, Np, Kp, n_ch, q;
   uint32_t C, k_full, k_last;
 };
 
 // Launchers; all enqueue on "s" and return cudaGetLastError().
-cudaError_t launch_offsets(const uint32_t* mask, uint32_t* toff_local, uint32_t* bsum,
-                           uint64_t n_wt, cudaStream_t s);
-cudaError_t launch_stream_compact(const StreamArgs& a, int W, cudaStream_t s);
-cudaError_t launch_reduce_update(const UpdateArgs& a, cudaStream_t s);
+cudaError_t launch_step_chunks(const FusedArgs& a, cudaStream_t s);
 cudaError_t launch_select(const SelectArgs& a, bool boot, cudaStream_t s);
 
 int num_sms();

@@ -17,7 +17,7 @@ LIB_PATH = os.path.join(HERE, "libscape.so")
 
 SCAPE_OK, SCAPE_EINVAL, SCAPE_ENOMEM, SCAPE_ECUDA, SCAPE_ESTATE = 0, -1, -2, -3, -4
 THETA, V, U, E, MASK, STEP = 0, 1, 2, 3, 4, 5
-PHASES = ("select_boot", "offsets", "stream_compact", "reduce_update", "select", "h2d")
+PHASES = ("select_boot", "step", "select_fallback", "h2d")
 
 # Symbols declared in include/scape.h (checked by the ABI test).
 EXPORTS = ("scape_create", "scape_step", "scape_step_host", "scape_mask", "scape_destroy",
@@ -41,7 +41,7 @@ class _Info(ctypes.Structure):
                 ("n_chunks", ctypes.c_uint64), ("chunks_per_worker", ctypes.c_uint64),
                 ("k_full", ctypes.c_uint32), ("k_last", ctypes.c_uint32), ("K", ctypes.c_uint64),
                 ("mask_words", ctypes.c_uint64), ("step", ctypes.c_int64),
-                ("device_bytes", ctypes.c_uint64)]
+                ("device_bytes", ctypes.c_uint64), ("select_fallbacks", ctypes.c_uint64)]
 
 
 _lib = None
