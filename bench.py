@@ -119,20 +119,22 @@ class ClockSampler:
                 "reasons": sorted(reasons)}
 
 
-def ncu_traffic(kernel: str, workload: str):
-    """Per-launch DRAM bytes from the committed ncu summary, if it was taken on
-    the current source of the kernel (else None)."""
+def ncu_traffic(kernel: str, N: int):
+    """Per-launch DRAM bytes (read + write) of the kernel from the committed ncu
+    summary: bytes per coordinate measured on a smaller capture of the same
+    kernel, times N (its traffic grows in proportion to the coordinates).
+    None when the summary was taken on another source of the kernel."""
     src = {"step_chunks": "k_fused.cu"}.get(kernel)
     path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
     if not src or not os.path.exists(path):
-        return None
+        return None, None
     h = hashlib.sha256(open(os.path.join(ROOT, "sparse_communication_distributed_gb300", "csrc",
                                          src), "rb").read()).hexdigest()[:16]
     for line in open(path):
         f = line.split()
-        if len(f) >= 4 and f[0] == kernel and f[1] == workload and f[3] == h:
-            return float(f[2])
-    return None
+        if len(f) >= 4 and f[0] == kernel and f[3] == h:
+            return float(f[2]) * N, f"scaled from an ncu capture on {f[1]}"
+    return None, None
 
 
 def oracle_sample(wl, density, n_chunks: int, steps: int):
@@ -280,6 +282,7 @@ def run_scape(args, wl, density):
         return
     peak, peak_kind = measured_peak()
     ab = alg_bytes(N, W, K)
+    traffic, traffic_src = ncu_traffic("step_chunks", N)
     a_ms, a_n = phases["step"]
     a_launch_ms = a_ms / max(a_n, 1)
     achieved = ab["step"] / (a_launch_ms * 1e-3) / 1e9
@@ -307,7 +310,7 @@ def run_scape(args, wl, density):
                      "frac_of_peak": step_gbs / peak, "peak_kind": peak_kind},
         "roofline": {"kernel": "step_chunks", "bound": "hbm", "achieved": achieved,
                      "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": ncu_traffic("step_chunks", wl.name),
+                     "traffic": traffic, "traffic_source": traffic_src,
                      "alg_bytes_per_launch": ab["step"], "launch_ms": a_launch_ms,
                      "peak_kind": f"{peak_kind} (hbm_gbs)"},
         "kernels_ms_per_step": {k: v[0] / args.steps for k, v in phases.items() if v[1]},
