@@ -162,6 +162,68 @@ int scape_profile(scape_handle* h, int enable);
  * the recorded events, then clears the record. */
 int scape_profile_read(scape_handle* h, double* ms, uint32_t* launches);
 
+/* ---- Allocation-free step ------------------------------------------------
+ * The SCAPE pages have no counterpart to this entry point; it exists for
+ * callers that may not call cudaMalloc: programs whose device memory is all
+ * owned by another allocator (a framework's caching pool, a fixed arena
+ * handed out at start-up) and programs that must not allocate inside their
+ * step loop because cudaMalloc can synchronise the device and changes the
+ * memory footprint they budgeted for.  Such a caller owns every buffer of
+ * the optimizer state and passes them in; the library allocates nothing.
+ *
+ * Buffers (all DEVICE pointers, 16-byte aligned, owned by the caller):
+ *   theta, v        N fp32 each
+ *   u, e            W rows of N fp32, row w starting at w * row_stride
+ *                   (row_stride a multiple of 4, >= N rounded up to 4)
+ *   mask_prev       M_{t-1}: ceil(N/32) words, bit j of word i = coordinate 32i+j
+ *   mask_next       M_t is written here (ceil(N/32) words; must differ from mask_prev)
+ *   vals            W rows of K fp32 (row stride vals_stride >= K): kept values
+ *   bbar, idx       K fp32 / K uint32: synchronized buffer and its coordinates
+ * K = sum over chunks of floor(density * chunk length), as scape_info gives.
+ * first_step != 0 means there is no M_{t-1} yet: the call first writes the
+ * step-0 mask into mask_prev, as scape_step does on a new handle.  Between
+ * calls the caller swaps mask_prev and mask_next.
+ *
+ * Scratch: the step needs one flag per chunk and a counter.  They live in a
+ * static device array inside the library, sized for at most 65536 chunks
+ * (256 KiB), which every GPU that loads the library holds until the process
+ * exits.  More chunks -> SCAPE_EINVAL.  Each call clears the part it uses
+ * with cudaMemsetAsync on "stream" (the array keeps the last call's
+ * contents otherwise).  All calls share the one array, so calls whose work
+ * overlaps on the GPU (different streams without ordering, or several
+ * threads) race on it: order them on one stream.
+ *
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) and sets the kernel's shared-memory limit; make
+ * that first call before any stream capture.  No call allocates device or
+ * pinned memory, and nothing calls cudaMalloc, cudaFree or an allocating
+ * library routine.
+ *
+ * Returns SCAPE_OK or SCAPE_EINVAL / SCAPE_ECUDA; the message is available
+ * from scape_last_error(NULL) on the calling thread.  The work is enqueued on
+ * "stream" and the call returns. */
+typedef struct {
+  const scape_layout* layout;
+  int W;
+  double density;
+  float beta1, beta2, lr, wd, eps;
+  float* theta;
+  float* v;
+  float* u;
+  float* e;
+  uint64_t row_stride;
+  uint32_t* mask_prev;
+  uint32_t* mask_next;
+  float* vals;
+  uint64_t vals_stride;
+  float* bbar;
+  uint32_t* idx;
+  int first_step;
+} scape_step_buffers;
+
+int scape_step_noalloc(const scape_step_buffers* buffers, const void* const* grad_ptrs,
+                       void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -168,6 +168,11 @@ bool mask_valid(const scape_handle* h, const std::vector<uint32_t>& m, std::stri
 
 }  // namespace
 
+namespace scape {
+// Sets the message scape_last_error(NULL) returns on this thread.
+void set_thread_error(const char* msg) { g_create_err = msg; }
+}  // namespace scape
+
 SCAPE_API int scape_create(const scape_layout* layout, int W, double density, float beta1,
                            float beta2, float lr, float wd, float eps, scape_handle** out) {
   if (!out) return fail(nullptr, SCAPE_EINVAL, "out is NULL");

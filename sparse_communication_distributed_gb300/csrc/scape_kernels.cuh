@@ -59,5 +59,6 @@ cudaError_t launch_step_chunks(const FusedArgs& a, cudaStream_t s);
 cudaError_t launch_select(const SelectArgs& a, bool boot, cudaStream_t s);
 
 int num_sms();
+void set_thread_error(const char* msg);
 
 }  // namespace scape

@@ -22,7 +22,7 @@ PHASES = ("select_boot", "step", "select_fallback", "h2d")
 # Symbols declared in include/scape.h (checked by the ABI test).
 EXPORTS = ("scape_create", "scape_step", "scape_step_host", "scape_mask", "scape_destroy",
            "scape_info", "scape_read_state", "scape_load_state", "scape_read_sparse",
-           "scape_last_error", "scape_profile", "scape_profile_read")
+           "scape_last_error", "scape_profile", "scape_profile_read", "scape_step_noalloc")
 
 
 class ScapeError(RuntimeError):
@@ -42,6 +42,18 @@ class _Info(ctypes.Structure):
                 ("k_full", ctypes.c_uint32), ("k_last", ctypes.c_uint32), ("K", ctypes.c_uint64),
                 ("mask_words", ctypes.c_uint64), ("step", ctypes.c_int64),
                 ("device_bytes", ctypes.c_uint64), ("select_fallbacks", ctypes.c_uint64)]
+
+
+class StepBuffers(ctypes.Structure):
+    """scape_step_buffers: caller-owned state for scape_step_noalloc."""
+    _fields_ = [("layout", ctypes.POINTER(_Layout)), ("W", ctypes.c_int),
+                ("density", ctypes.c_double), ("beta1", ctypes.c_float),
+                ("beta2", ctypes.c_float), ("lr", ctypes.c_float), ("wd", ctypes.c_float),
+                ("eps", ctypes.c_float), ("theta", ctypes.c_void_p), ("v", ctypes.c_void_p),
+                ("u", ctypes.c_void_p), ("e", ctypes.c_void_p), ("row_stride", ctypes.c_uint64),
+                ("mask_prev", ctypes.c_void_p), ("mask_next", ctypes.c_void_p),
+                ("vals", ctypes.c_void_p), ("vals_stride", ctypes.c_uint64),
+                ("bbar", ctypes.c_void_p), ("idx", ctypes.c_void_p), ("first_step", ctypes.c_int)]
 
 
 _lib = None
@@ -73,6 +85,7 @@ def load_library(path: str = LIB_PATH):
     lib.scape_profile.argtypes = [vp, i32]
     lib.scape_profile_read.argtypes = [vp, ctypes.POINTER(ctypes.c_double),
                                        ctypes.POINTER(ctypes.c_uint32)]
+    lib.scape_step_noalloc.argtypes = [ctypes.POINTER(StepBuffers), ctypes.POINTER(vp), vp]
     _lib = lib
     return lib
 
@@ -206,3 +219,23 @@ class Scape:
         n = (ctypes.c_uint32 * len(PHASES))()
         self._check(self.lib.scape_profile_read(self.h, ms, n))
         return {p: (ms[i], n[i]) for i, p in enumerate(PHASES)}
+
+
+def step_noalloc(numel, chunk: int, W: int, density: float, hyper, buffers: dict, grads,
+                 first_step: bool, stream=None) -> None:
+    """scape_step_noalloc on caller-owned device tensors.  ``hyper`` is
+    (beta1, beta2, lr, wd, eps); ``buffers`` maps theta, v, u, e, mask_prev,
+    mask_next, vals, bbar, idx to tensors and row_stride, vals_stride to ints."""
+    lib = load_library()
+    arr = np.ascontiguousarray(numel, dtype=np.uint64)
+    lay = _Layout(arr.size, arr.ctypes.data_as(ctypes.POINTER(ctypes.c_uint64)), chunk)
+    b1, b2, lr, wd, eps = hyper
+    sb = StepBuffers(ctypes.pointer(lay), W, density, b1, b2, lr, wd, eps,
+                     *[_ptr(buffers[k]) for k in ("theta", "v", "u", "e")], buffers["row_stride"],
+                     _ptr(buffers["mask_prev"]), _ptr(buffers["mask_next"]), _ptr(buffers["vals"]),
+                     buffers["vals_stride"], _ptr(buffers["bbar"]), _ptr(buffers["idx"]),
+                     1 if first_step else 0)
+    gp = (ctypes.c_void_p * len(grads))(*[_ptr(g) for g in grads])
+    rc = lib.scape_step_noalloc(ctypes.byref(sb), gp, _stream_handle(stream))
+    if rc != SCAPE_OK:
+        raise ScapeError(rc, lib.scape_last_error(None).decode())
