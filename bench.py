@@ -44,6 +44,8 @@ def parse():
     ap.add_argument("--workload", default=synth.BENCH_WORKLOAD, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--density", type=float, default=None)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-pageable", action="store_true",
+                    help="also time the staged-copy path with pageable host gradients")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
 
@@ -51,6 +53,39 @@ def parse():
 def dist_env():
     return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
             int(os.environ.get("LOCAL_RANK", 0)))
+
+
+class Ranks:
+    """Process-group plumbing of the replica runs: barrier, max over ranks.
+    ``backend`` None means a single process (no group)."""
+
+    def __init__(self, backend: str | None, device=None):
+        self.dist = None
+        self.device = device
+        if backend:
+            import torch.distributed as dist
+            if backend == "nccl":
+                dist.init_process_group("nccl", device_id=device)
+            else:
+                dist.init_process_group(backend)
+            self.dist = dist
+
+    def barrier(self):
+        if self.dist:
+            self.dist.barrier()
+
+    def max(self, x: float) -> float:
+        if not self.dist:
+            return x
+        import torch
+        t = torch.tensor([x], dtype=torch.float64,
+                         device=self.device if self.device is not None else "cpu")
+        self.dist.all_reduce(t, op=self.dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.dist:
+            self.dist.destroy_process_group()
 
 
 def measured_peak():
@@ -185,15 +220,8 @@ def run_scape(args, wl, density):
     rank, world, local = dist_env()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    pg = None
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=dev)
-        pg = dist
-
-    def barrier():
-        if pg:
-            pg.barrier()
+    ranks = Ranks("nccl" if world > 1 else None, dev)
+    barrier = ranks.barrier
 
     N, W = wl.N, wl.W
     sc = Scape.for_workload(wl, density)
@@ -239,37 +267,39 @@ def run_scape(args, wl, density):
     sc.profile(False)
     clk = clocks.stop()
 
-    ms_max = ms
-    if pg:
-        t = torch.tensor([ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms_max = float(t.item())
-    ms_per_step = ms_max / args.steps
+    ms_per_step = ranks.max(ms) / args.steps
 
     # end to end through the public API: host gradients in, mask out
     e2e = None
     if not args.no_e2e:
-        host = [batches[0][w].cpu().pin_memory() for w in range(W)]
         out = torch.empty(sc.info["mask_words"], dtype=torch.int32).pin_memory()
         e2e_steps = min(args.steps, 5)
-        sc.step_host(host, stream)
-        sc.mask_into(out)
-        barrier()
-        torch.cuda.synchronize()
-        t0 = time.perf_counter()
-        for _ in range(e2e_steps):
+
+        def timed_host_steps(host):
             sc.step_host(host, stream)
             sc.mask_into(out)
-        torch.cuda.synchronize()
-        dt = time.perf_counter() - t0
-        if pg:
-            t = torch.tensor([dt], device=dev)
-            pg.all_reduce(t, op=pg.ReduceOp.MAX)
-            dt = float(t.item())
+            barrier()
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            for _ in range(e2e_steps):
+                sc.step_host(host, stream)
+                sc.mask_into(out)
+            torch.cuda.synchronize()
+            return ranks.max(time.perf_counter() - t0)
+
+        pinned = [batches[0][w].cpu().pin_memory() for w in range(W)]
+        dt = timed_host_steps(pinned)
+        del pinned
         e2e = {"value": world * N * e2e_steps / dt, "unit": "params/s",
                "h2d_bytes_per_step": W * N * 2, "d2h_bytes_per_step": sc.info["mask_words"] * 4,
-               "ms_per_step": dt / e2e_steps * 1e3, "steps": e2e_steps}
-        del host, out
+               "ms_per_step": dt / e2e_steps * 1e3, "steps": e2e_steps,
+               "host_buffers": "pinned, read in place by the step kernel"}
+        if args.e2e_pageable:
+            pageable = [batches[0][w].cpu() for w in range(W)]
+            dtp = timed_host_steps(pageable)
+            e2e["pageable_staged_ms_per_step"] = dtp / e2e_steps * 1e3
+            del pageable
+        del out
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -279,6 +309,7 @@ def run_scape(args, wl, density):
                          f"4 steps incl. step 0, {dt:.1f} s; single-threaded C++ oracle"}
 
     if rank != 0:
+        ranks.close()
         return
     peak, peak_kind = measured_peak()
     ab = alg_bytes(N, W, K)
@@ -321,8 +352,7 @@ def run_scape(args, wl, density):
         "cpu_baseline": cpu,
     }
     print(json.dumps(line), flush=True)
-    if pg:
-        pg.destroy_process_group()
+    ranks.close()
 
 
 def main():

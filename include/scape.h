@@ -110,10 +110,13 @@ int scape_create(const scape_layout* layout, int W, double density, float beta1,
  * completed on "stream".  Enqueues the step's kernels and returns. */
 int scape_step(scape_handle* h, const void* const* grad_ptrs, void* stream);
 
-/* The same step from HOST gradients: W host pointers to N bf16 each (pinned
- * memory gives full copy speed).  The first call allocates a W x N bf16
- * device staging buffer owned by the handle; each call enqueues the W
- * host-to-device copies and the step on "stream" and returns. */
+/* The same step from HOST gradients: W host pointers to N bf16 each,
+ * borrowed until the step has completed on "stream".  Page-locked buffers
+ * (cudaHostAlloc / cudaHostRegister, 16-byte aligned) are read by the step
+ * kernel in place over the CPU-GPU link: no copy, no staging buffer.  Other
+ * host memory is first copied (cudaMemcpyAsync per worker) into a W x N bf16
+ * device staging buffer that the first such call allocates and the handle
+ * owns.  Enqueues the work on "stream" and returns. */
 int scape_step_host(scape_handle* h, const void* const* host_grad_ptrs, void* stream);
 
 /* Copy M_t, the mask built by the last step (applied at the next one), into

@@ -376,12 +376,35 @@ SCAPE_API int scape_step(scape_handle* h, const void* const* grad_ptrs, void* st
   return step_device(h, g.data(), static_cast<cudaStream_t>(stream));
 }
 
+// Device-visible address of a page-locked host buffer, or nullptr when the
+// buffer is ordinary (pageable) host memory.
+static const void* pinned_device_ptr(const void* host) {
+  cudaPointerAttributes at{};
+  if (cudaPointerGetAttributes(&at, host) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  if (at.type != cudaMemoryTypeHost || !at.devicePointer) return nullptr;
+  return at.devicePointer;
+}
+
 SCAPE_API int scape_step_host(scape_handle* h, const void* const* host_grad_ptrs, void* stream) {
   if (!h) return SCAPE_EINVAL;
   int rc = check_grad_ptrs(h, host_grad_ptrs, false);
   if (rc) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
+  std::vector<const uint16_t*> g(h->W);
+  // Page-locked buffers: the step kernel reads them in place over the
+  // CPU-GPU link (each gradient is read once), no copy and no staging.
+  bool direct = true;
+  for (int w = 0; w < h->W && direct; w++) {
+    const void* d = pinned_device_ptr(host_grad_ptrs[w]);
+    if (!d || (reinterpret_cast<uintptr_t>(d) & 15)) direct = false;
+    else g[w] = static_cast<const uint16_t*>(d);
+  }
+  if (direct) return step_device(h, g.data(), s);
+
   const uint64_t per = (h->N + 7) / 8 * 8;  // keep every worker's slice 16-byte aligned
   if (!h->stage) {
     if ((e = cudaMalloc(&h->stage, (uint64_t)h->W * per * sizeof(uint16_t))) != cudaSuccess) {
@@ -392,7 +415,6 @@ SCAPE_API int scape_step_host(scape_handle* h, const void* const* host_grad_ptrs
     }
     h->device_bytes += (uint64_t)h->W * per * sizeof(uint16_t);
   }
-  std::vector<const uint16_t*> g(h->W);
   {
     PhaseTimer pt(h, SCAPE_PH_H2D, s);
     for (int w = 0; w < h->W; w++) {

@@ -172,15 +172,20 @@ def test_resume_is_bit_identical():
         c.close()
 
 
-def test_step_host_matches_step():
+@pytest.mark.parametrize("memory", ["pinned", "pageable"])
+def test_step_host_matches_step(memory):
+    # pinned buffers are read in place by the kernel; pageable ones are staged
     wl = synth.tiny(20000, 2, 1024, 0.1, seed=4)
     a, b = GpuRun(wl, 0.1), GpuRun(wl, 0.1)
     try:
         for t in range(3):
             gr = np.stack([synth.cpu().grads(wl, w, t, n=wl.N) for w in range(2)])
             a.step(gr)
-            pinned = [torch.from_numpy(gr[w].view(np.int16)).pin_memory() for w in range(2)]
-            b.sc.step_host(pinned)
+            if memory == "pinned":
+                host = [torch.from_numpy(gr[w].view(np.int16)).pin_memory() for w in range(2)]
+            else:
+                host = [np.ascontiguousarray(gr[w]) for w in range(2)]
+            b.sc.step_host(host)
         torch.cuda.synchronize()
         for f in (THETA, V, MASK):
             assert np.array_equal(a.sc.read(f).view(np.uint32), b.sc.read(f).view(np.uint32))
