@@ -72,6 +72,9 @@ def load(path: str = SO):
     lib.oracle_get_sparse.argtypes = [ctypes.c_void_p, ctypes.c_int, _f32p, _u64p]
     lib.oracle_get_sparse.restype = ctypes.c_uint64
     lib.oracle_topk.argtypes = [_f32p, ctypes.c_uint32, ctypes.c_uint32, _u8p]
+    lib.oracle_dense_adams_step.argtypes = [_f32p, _f32p, _f32p, _u16p, ctypes.c_uint64,
+                                            ctypes.c_int, ctypes.c_float, ctypes.c_float,
+                                            ctypes.c_float, ctypes.c_float, ctypes.c_float]
     _libs[path] = lib
     return lib
 
@@ -166,6 +169,19 @@ def topk(a: np.ndarray, k: int, lib_path: str = SO) -> np.ndarray:
     if lib.oracle_topk(_p(a, _f32p), a.size, k, _p(out, _u8p)) != 0:
         raise ValueError("oracle_topk rejected its arguments")
     return out
+
+
+def dense_adams_step(theta: np.ndarray, m: np.ndarray, v: np.ndarray, grads: np.ndarray,
+                     beta1=0.9, beta2=0.95, lr=1e-3, wd=0.1, eps=1e-8, lib_path: str = SO) -> None:
+    """The oracle's dense AdamS step, in place on fp32 theta, m, v; grads (W, n) bf16 bits."""
+    lib = load(lib_path)
+    g = np.ascontiguousarray(grads, dtype=np.uint16)
+    W, n = g.shape
+    for a in (theta, m, v):
+        assert a.dtype == np.float32 and a.flags.c_contiguous and a.size == n
+    if lib.oracle_dense_adams_step(_p(theta, _f32p), _p(m, _f32p), _p(v, _f32p), _p(g, _u16p), n,
+                                   W, beta1, beta2, lr, wd, eps) != 0:
+        raise ValueError("oracle_dense_adams_step rejected its arguments")
 
 
 def pack_bits(m: np.ndarray) -> np.ndarray:

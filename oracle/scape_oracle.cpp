@@ -357,3 +357,32 @@ OR_API int oracle_topk(const float* a, uint32_t len, uint32_t k, uint8_t* keep) 
   select_topk(a, len, k, keep);
   return 0;
 }
+
+/* Dense AdamS under data parallelism, the comparator the SCAPE pages measure
+ * against (abstract: "3.26x speedup per step compared to dense AdamS";
+ * gist.science technical summary §4).  Every worker's full gradient is
+ * averaged (the dense all-reduce, workers summed in order 0..W-1), then one
+ * AdamS update, whose second moment is the EMA of the squared momentum:
+ *   gbar  = (g_0 + ... + g_{W-1}) * (1/W)
+ *   m     = b1*m + (1-b1)*gbar
+ *   v     = b2*v + (1-b2)*(m*m)
+ *   theta = theta - lr*(m/(sqrt(v)+eps) + wd*theta)
+ * fp32 with the same conventions as the SCAPE step above.  grads[W][n]. */
+OR_API int oracle_dense_adams_step(float* theta, float* m, float* v, const uint16_t* grads,
+                                   uint64_t n, int W, float b1, float b2, float lr, float wd,
+                                   float eps) {
+  if (!theta || !m || !v || !grads || W < 1) return -1;
+  const float c1 = 1.0f - b1;
+  const float c2 = 1.0f - b2;
+  const float invW = 1.0f / (float)W;
+  for (uint64_t i = 0; i < n; i++) {
+    float s = bf16_to_f32(grads[i]);
+    for (int w = 1; w < W; w++) s = s + bf16_to_f32(grads[(uint64_t)w * n + i]);
+    const float gbar = s * invW;
+    m[i] = (b1 * m[i]) + (c1 * gbar);
+    v[i] = (b2 * v[i]) + (c2 * (m[i] * m[i]));
+    const float q = m[i] / (std::sqrt(v[i]) + eps);
+    theta[i] = theta[i] - (lr * (q + (wd * theta[i])));
+  }
+  return 0;
+}

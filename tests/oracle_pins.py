@@ -286,8 +286,60 @@ def pin_offmask_decay(lib: str = SO) -> None:
                                rtol=2e-6)
 
 
+# ---------------------------------------------------------------- dense AdamS
+
+def pin_dense_adams_single_worker(lib: str = SO) -> None:
+    """Dense AdamS with W = 1 is the SCAPE step at W = 1, density 1, bit for
+    bit: gbar = g, m = u, bbar = u (1/W = 1 is exact)."""
+    wl = synth.tiny(2048, 1, 512, 1.0, seed=31)
+    o = oracle.Oracle.for_workload(wl, 1.0, lib_path=lib)
+    th0 = synth.cpu().theta0(wl, o.index)
+    o.set(oracle.THETA, th0)
+    th, m, v = th0.copy(), np.zeros(o.n, np.float32), np.zeros(o.n, np.float32)
+    for t in range(4):
+        g = np.stack([synth.cpu().grads(wl, 0, t, idx=o.index)])
+        o.step(g)
+        oracle.dense_adams_step(th, m, v, g, wl.beta1, wl.beta2, wl.lr, wl.wd, wl.eps, lib_path=lib)
+    assert np.array_equal(th.view(np.uint32), o.get(oracle.THETA).view(np.uint32))
+    assert np.array_equal(v.view(np.uint32), o.get(oracle.V).view(np.uint32))
+    assert np.array_equal(m.view(np.uint32), o.get(oracle.U, 0).view(np.uint32))
+
+
+def pin_dense_adams_matches_scape_density1(lib: str = SO) -> None:
+    """W = 4: the mean of per-worker momenta (SCAPE at density 1) equals the
+    momentum of the mean gradient (dense AdamS) up to fp32 rounding."""
+    wl = synth.tiny(4096, 4, 1024, 1.0, seed=32)
+    o = oracle.Oracle.for_workload(wl, 1.0, lib_path=lib)
+    th0 = synth.cpu().theta0(wl, o.index)
+    o.set(oracle.THETA, th0)
+    th, m, v = th0.copy(), np.zeros(o.n, np.float32), np.zeros(o.n, np.float32)
+    for t in range(5):
+        g = np.stack([synth.cpu().grads(wl, w, t, idx=o.index) for w in range(4)])
+        o.step(g)
+        oracle.dense_adams_step(th, m, v, g, wl.beta1, wl.beta2, wl.lr, wl.wd, wl.eps, lib_path=lib)
+    np.testing.assert_allclose(v, o.get(oracle.V), rtol=2e-5, atol=1e-20)
+    np.testing.assert_allclose(th, o.get(oracle.THETA), rtol=0, atol=5e-8)
+
+
+def pin_dense_adams_constant_gradient(lib: str = SO) -> None:
+    """Constant gradient c: m_t = (1 - b1^(t+1)) c, v_t = sum_s b2^(t-s) (1-b2) m_s^2."""
+    n, W = 256, 3
+    c = np.float32(0.0078125)
+    g = np.full((W, n), c.view(np.uint32) >> 16, np.uint16)
+    th, m, v = np.zeros(n, np.float32), np.zeros(n, np.float32), np.zeros(n, np.float32)
+    vr = 0.0
+    for t in range(6):
+        oracle.dense_adams_step(th, m, v, g, lib_path=lib)
+        mr = (1 - 0.9 ** (t + 1)) * float(c)
+        vr = 0.95 * vr + 0.05 * mr * mr
+        np.testing.assert_allclose(m, mr, rtol=3e-6)
+        np.testing.assert_allclose(v, vr, rtol=1e-5)
+
+
 ALL_PINS = [
     pin_dense_adams, pin_single_worker_identity, pin_momentum_closed_form, pin_fixed_sum_order,
     pin_accumulator_split, pin_error_feedback_conservation, pin_delayed_mask,
     pin_partitioned_topk, pin_topk_against_sort, pin_shard_geometry, pin_offmask_decay,
+    pin_dense_adams_single_worker, pin_dense_adams_matches_scape_density1,
+    pin_dense_adams_constant_gradient,
 ]

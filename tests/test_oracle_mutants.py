@@ -37,6 +37,13 @@ MUTANTS = [
     ("mask not delayed", "if (o.t == 0) {", "if (true) {"),
     ("bias correction added", "float q = bb / (std::sqrt(o.v[i]) + o.eps);",
      "float q = (bb / (1.0f - std::pow(o.b1, (float)(o.t + 1)))) / (std::sqrt(o.v[i]) + o.eps);"),
+    ("dense: mean misses 1/W", "const float gbar = s * invW;", "const float gbar = s;"),
+    ("dense: second moment from the gradient", "v[i] = (b2 * v[i]) + (c2 * (m[i] * m[i]));",
+     "v[i] = (b2 * v[i]) + (c2 * (gbar * gbar));"),
+    ("dense: momentum uses beta2", "m[i] = (b1 * m[i]) + (c1 * gbar);",
+     "m[i] = (b2 * m[i]) + (c1 * gbar);"),
+    ("dense: weight decay dropped", "theta[i] = theta[i] - (lr * (q + (wd * theta[i])));",
+     "theta[i] = theta[i] - (lr * q);"),
 ]
 
 
