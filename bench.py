@@ -47,6 +47,7 @@ def parse():
     ap.add_argument("--e2e-pageable", action="store_true",
                     help="also time the staged-copy path with pageable host gradients")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-dense", action="store_true", help="skip the dense AdamS comparator")
     return ap.parse_args()
 
 
@@ -301,6 +302,35 @@ def run_scape(args, wl, density):
             del pageable
         del out
 
+    # the pages' comparator on the same layout and gradients: dense AdamS
+    dense = None
+    if not args.no_dense:
+        from sparse_communication_distributed_gb300.scape import dense_adams_step
+        th_d = torch.empty(N, dtype=torch.float32, device=dev)
+        synth.gpu().theta_into(wl, th_d)
+        m_d = torch.zeros(N, dtype=torch.float32, device=dev)
+        v_d = torch.zeros(N, dtype=torch.float32, device=dev)
+        hyper = dict(beta1=wl.beta1, beta2=wl.beta2, lr=wl.lr, wd=wl.wd, eps=wl.eps)
+        for i in range(args.warmup):
+            dense_adams_step(th_d, m_d, v_d, batches[i % n_batches], stream=stream, **hyper)
+        barrier()
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        for i in range(args.steps):
+            dense_adams_step(th_d, m_d, v_d, batches[i % n_batches], stream=stream, **hyper)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        d_ms = ranks.max(ev0.elapsed_time(ev1)) / args.steps
+        d_bytes = N * (2 * W + 24)
+        dense = {"ms_per_step": d_ms, "params_per_s": world * N / (d_ms * 1e-3),
+                 "alg_bytes_per_step": d_bytes, "achieved_gbs": d_bytes / (d_ms * 1e-3) / 1e9,
+                 "exchange_bytes_per_worker": {
+                     "dense_allreduce_fp32": 4 * N,
+                     "scape_sparse_fp32_plus_mask": 4 * K + N // (8 * W)},
+                 "note": "one GPU: both steps' exchanges are emulated in HBM, so this compares "
+                         "memory work, not network time"}
+        del th_d, m_d, v_d
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         rate, dt, n, nc = oracle_sample(wl, density, 64 if N > 1 << 24 else 16, 4)
@@ -349,6 +379,7 @@ def run_scape(args, wl, density):
         "select_fallback_chunks": sc._info()["select_fallbacks"],
         "clocks": clk,
         "e2e": e2e,
+        "dense_adams": dense,
         "cpu_baseline": cpu,
     }
     print(json.dumps(line), flush=True)

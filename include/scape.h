@@ -165,6 +165,24 @@ int scape_profile(scape_handle* h, int enable);
  * the recorded events, then clears the record. */
 int scape_profile_read(scape_handle* h, double* ms, uint32_t* launches);
 
+/* ---- Dense AdamS baseline --------------------------------------------------
+ * The comparator of the SCAPE pages ("3.26x speedup per step compared to
+ * dense AdamS": abstract; gist.science technical summary §4): dense data
+ * parallelism, where every worker's full gradient is averaged (the dense
+ * all-reduce, here a fixed-order sum over the W replicas) and one AdamS update
+ * follows on every coordinate:
+ *   gbar = (g_0 + ... + g_{W-1}) * (1/W);  m = b1*m + (1-b1)*gbar;
+ *   v = b2*v + (1-b2)*(m*m);  theta = theta - lr*(m/(sqrt(v)+eps) + wd*theta)
+ * (fp32, no fused multiply-add, correctly rounded sqrt and /).
+ * theta, m, v: N fp32 each, DEVICE, 16-byte aligned, caller-owned and updated
+ * in place.  grad_ptrs: HOST array of W DEVICE pointers to N bf16 each
+ * (16-byte aligned), read-only.  Allocates nothing; enqueues one kernel on
+ * "stream" and returns.  SCAPE_EINVAL on bad arguments (message from
+ * scape_last_error(NULL)), SCAPE_ECUDA on a launch error. */
+int scape_dense_adams_step(float* theta, float* m, float* v, const void* const* grad_ptrs, int W,
+                           uint64_t N, float beta1, float beta2, float lr, float wd, float eps,
+                           void* stream);
+
 /* ---- Allocation-free step ------------------------------------------------
  * The SCAPE pages have no counterpart to this entry point; it exists for
  * callers that may not call cudaMalloc: programs whose device memory is all

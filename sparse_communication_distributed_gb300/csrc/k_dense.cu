@@ -1,0 +1,137 @@
+// Dense AdamS under data parallelism: the comparator of the SCAPE pages
+// (abstract: "3.26x speedup per step compared to dense AdamS"; gist.science
+// technical summary §4).  Every worker's full gradient is averaged -- the
+// dense all-reduce, emulated as a fixed-order sum over the W gradient
+// replicas -- and one AdamS update follows:
+//   gbar  = (g_0 + ... + g_{W-1}) * (1/W)        left to right
+//   m     = b1*m + c1*gbar                        c1 = 1 - b1 (fp32)
+//   v     = b2*v + c2*(m*m)                       c2 = 1 - b2 (fp32)
+//   theta = theta - lr*(m/(sqrt(v)+eps) + wd*theta)
+// One thread per 8 consecutive coordinates: W 16-byte gradient loads and two
+// 16-byte loads and stores each of theta, m and v.  HBM traffic per
+// coordinate: 2W + 24 bytes, all compulsory.
+#include <cstdarg>
+#include <cstdio>
+
+#include "../../include/scape.h"
+#include "scape_device.cuh"
+#include "scape_kernels.cuh"
+
+#define SCAPE_API extern "C" __attribute__((visibility("default")))
+
+namespace scape {
+namespace {
+
+struct DenseArgs {
+  const uint16_t* grads[kMaxW];
+  float* theta;
+  float* m;
+  float* v;
+  uint64_t N;
+  int W;
+  float b1, c1, b2, c2, lr, wd, eps, invW;
+};
+
+__device__ __forceinline__ void unpack8(const uint4 r, float f[8]) {
+  f[0] = bf16lo(r.x); f[1] = bf16hi(r.x); f[2] = bf16lo(r.y); f[3] = bf16hi(r.y);
+  f[4] = bf16lo(r.z); f[5] = bf16hi(r.z); f[6] = bf16lo(r.w); f[7] = bf16hi(r.w);
+}
+
+__device__ __forceinline__ void update1(const DenseArgs& p, float s, float& th, float& m,
+                                        float& v) {
+  const float gbar = s * p.invW;
+  m = (p.b1 * m) + (p.c1 * gbar);
+  v = (p.b2 * v) + (p.c2 * (m * m));
+  const float q = m / (sqrtf(v) + p.eps);
+  th = th - (p.lr * (q + (p.wd * th)));
+}
+
+__global__ __launch_bounds__(256) void dense_adams(const DenseArgs p) {
+  const uint64_t ngroups = (p.N + 7) / 8;
+  const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+  for (uint64_t gi = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; gi < ngroups; gi += stride) {
+    const uint64_t i0 = gi * 8;
+    if (i0 + 8 <= p.N) {
+      float s[8], x[8];
+      unpack8(ld_stream_u4(p.grads[0] + i0), s);
+      for (int w = 1; w < p.W; w++) {
+        unpack8(ld_stream_u4(p.grads[w] + i0), x);
+#pragma unroll
+        for (int j = 0; j < 8; j++) s[j] = s[j] + x[j];
+      }
+      float4* tp = reinterpret_cast<float4*>(p.theta + i0);
+      float4* mp = reinterpret_cast<float4*>(p.m + i0);
+      float4* vp = reinterpret_cast<float4*>(p.v + i0);
+      float4 t0 = tp[0], t1 = tp[1], m0 = mp[0], m1 = mp[1], v0 = vp[0], v1 = vp[1];
+      update1(p, s[0], t0.x, m0.x, v0.x);
+      update1(p, s[1], t0.y, m0.y, v0.y);
+      update1(p, s[2], t0.z, m0.z, v0.z);
+      update1(p, s[3], t0.w, m0.w, v0.w);
+      update1(p, s[4], t1.x, m1.x, v1.x);
+      update1(p, s[5], t1.y, m1.y, v1.y);
+      update1(p, s[6], t1.z, m1.z, v1.z);
+      update1(p, s[7], t1.w, m1.w, v1.w);
+      tp[0] = t0; tp[1] = t1; mp[0] = m0; mp[1] = m1; vp[0] = v0; vp[1] = v1;
+    } else {
+      for (uint64_t i = i0; i < p.N; i++) {
+        float s = bf16f(p.grads[0][i]);
+        for (int w = 1; w < p.W; w++) s = s + bf16f(p.grads[w][i]);
+        update1(p, s, p.theta[i], p.m[i], p.v[i]);
+      }
+    }
+  }
+}
+
+int fail(int code, const char* fmt, ...) {
+  char buf[256];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  set_thread_error(buf);
+  return code;
+}
+
+bool aligned16(const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0; }
+
+}  // namespace
+}  // namespace scape
+
+SCAPE_API int scape_dense_adams_step(float* theta, float* m, float* v,
+                                     const void* const* grad_ptrs, int W, uint64_t N,
+                                     float beta1, float beta2, float lr, float wd, float eps,
+                                     void* stream) {
+  using namespace scape;
+  if (W < 1 || W > kMaxW) return fail(SCAPE_EINVAL, "W=%d outside [1, %d]", W, kMaxW);
+  if (N == 0) return fail(SCAPE_EINVAL, "N must be > 0");
+  if (!theta || !m || !v || !aligned16(theta) || !aligned16(m) || !aligned16(v))
+    return fail(SCAPE_EINVAL, "theta, m and v must be 16-byte aligned device pointers");
+  if (!grad_ptrs) return fail(SCAPE_EINVAL, "grad_ptrs is NULL");
+  if (!(eps > 0.0f)) return fail(SCAPE_EINVAL, "eps must be > 0");
+  DenseArgs a{};
+  for (int w = 0; w < W; w++) {
+    if (!grad_ptrs[w] || !aligned16(grad_ptrs[w]))
+      return fail(SCAPE_EINVAL, "grad_ptrs[%d] must be a 16-byte aligned device pointer", w);
+    a.grads[w] = static_cast<const uint16_t*>(grad_ptrs[w]);
+  }
+  a.theta = theta;
+  a.m = m;
+  a.v = v;
+  a.N = N;
+  a.W = W;
+  a.b1 = beta1;
+  a.c1 = 1.0f - beta1;
+  a.b2 = beta2;
+  a.c2 = 1.0f - beta2;
+  a.lr = lr;
+  a.wd = wd;
+  a.eps = eps;
+  a.invW = 1.0f / (float)W;
+  uint64_t groups = (N + 7) / 8;
+  uint64_t grid = (groups + 255) / 256;
+  const uint64_t cap = (uint64_t)num_sms() * 8;
+  if (grid > cap) grid = cap;
+  dense_adams<<<(unsigned)grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(a);
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? SCAPE_OK : fail(SCAPE_ECUDA, "dense_adams: %s", cudaGetErrorString(e));
+}

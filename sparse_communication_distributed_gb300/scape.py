@@ -22,7 +22,8 @@ PHASES = ("select_boot", "step", "select_fallback", "h2d")
 # Symbols declared in include/scape.h (checked by the ABI test).
 EXPORTS = ("scape_create", "scape_step", "scape_step_host", "scape_mask", "scape_destroy",
            "scape_info", "scape_read_state", "scape_load_state", "scape_read_sparse",
-           "scape_last_error", "scape_profile", "scape_profile_read", "scape_step_noalloc")
+           "scape_last_error", "scape_profile", "scape_profile_read", "scape_step_noalloc",
+           "scape_dense_adams_step")
 
 
 class ScapeError(RuntimeError):
@@ -86,6 +87,9 @@ def load_library(path: str = LIB_PATH):
     lib.scape_profile_read.argtypes = [vp, ctypes.POINTER(ctypes.c_double),
                                        ctypes.POINTER(ctypes.c_uint32)]
     lib.scape_step_noalloc.argtypes = [ctypes.POINTER(StepBuffers), ctypes.POINTER(vp), vp]
+    f32 = ctypes.c_float
+    lib.scape_dense_adams_step.argtypes = [vp, vp, vp, ctypes.POINTER(vp), i32, u64, f32, f32, f32,
+                                           f32, f32, vp]
     _lib = lib
     return lib
 
@@ -237,5 +241,16 @@ def step_noalloc(numel, chunk: int, W: int, density: float, hyper, buffers: dict
                      1 if first_step else 0)
     gp = (ctypes.c_void_p * len(grads))(*[_ptr(g) for g in grads])
     rc = lib.scape_step_noalloc(ctypes.byref(sb), gp, _stream_handle(stream))
+    if rc != SCAPE_OK:
+        raise ScapeError(rc, lib.scape_last_error(None).decode())
+
+
+def dense_adams_step(theta, m, v, grads, beta1=0.9, beta2=0.95, lr=1e-3, wd=0.1, eps=1e-8,
+                     stream=None) -> None:
+    """scape_dense_adams_step on device tensors (theta, m, v fp32; grads W x bf16)."""
+    lib = load_library()
+    gp = (ctypes.c_void_p * len(grads))(*[_ptr(g) for g in grads])
+    rc = lib.scape_dense_adams_step(_ptr(theta), _ptr(m), _ptr(v), gp, len(grads), theta.numel(),
+                                    beta1, beta2, lr, wd, eps, _stream_handle(stream))
     if rc != SCAPE_OK:
         raise ScapeError(rc, lib.scape_last_error(None).decode())
