@@ -48,6 +48,9 @@ def parse():
                     help="also time the staged-copy path with pageable host gradients")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-dense", action="store_true", help="skip the dense AdamS comparator")
+    ap.add_argument("--mask-stats", action="store_true",
+                    help="report mask overlap and the fill-in of per-worker global top-k")
+    ap.add_argument("--workers", type=int, default=None, help="override W of the workload")
     return ap.parse_args()
 
 
@@ -302,6 +305,14 @@ def run_scape(args, wl, density):
             del pageable
         del out
 
+    mstats = None
+    if args.mask_stats:
+        st = sc.mask_stats()
+        mstats = {"kept": st["kept"], "overlap_prev_frac": st["overlap_prev"] / st["kept"],
+                  "union_global_topk": st["union_global_topk"],
+                  "fill_in": st["union_global_topk"] / st["kept"],
+                  "step": sc.step_count}
+
     # the pages' comparator on the same layout and gradients: dense AdamS
     dense = None
     if not args.no_dense:
@@ -380,6 +391,7 @@ def run_scape(args, wl, density):
         "clocks": clk,
         "e2e": e2e,
         "dense_adams": dense,
+        "mask_stats": mstats,
         "cpu_baseline": cpu,
     }
     print(json.dumps(line), flush=True)
@@ -389,6 +401,9 @@ def run_scape(args, wl, density):
 def main():
     args = parse()
     wl = synth.WORKLOADS[args.workload]
+    if args.workers is not None:
+        import dataclasses
+        wl = dataclasses.replace(wl, W=args.workers)
     density = args.density if args.density is not None else wl.densities[0]
     if args.impl == "reference":
         run_reference(args, wl, density)

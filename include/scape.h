@@ -165,6 +165,28 @@ int scape_profile(scape_handle* h, int enable);
  * the recorded events, then clears the record. */
 int scape_profile_read(scape_handle* h, double* ms, uint32_t* launches);
 
+/* ---- Mask diagnostics -------------------------------------------------------
+ * Two properties the SCAPE pages build on (gist.science technical summary
+ * §2): the top-k structure of the first moment is stable from one step to the
+ * next (which is what lets the mask be used one step late), and letting every
+ * worker select over the whole vector instead of its own shard "fills in" the
+ * global mask as W grows.  After a step:
+ *   kept              = |M_t| (= K)
+ *   overlap_prev      = |M_t AND M_{t-1}|: coordinates kept two steps running
+ *   union_global_topk = | OR_w S_w |, S_w = worker w's own top-k_c of |a_w| in
+ *                       EVERY chunk (not only its shard), from the same
+ *                       accumulators; the partitioned rule keeps K of them.
+ * Waits for the last step; the first call allocates 2 masks of diagnostics
+ * buffers on the device (freed with the handle).  SCAPE_ESTATE before the
+ * first step. */
+typedef struct {
+  uint64_t kept;
+  uint64_t overlap_prev;
+  uint64_t union_global_topk;
+} scape_mask_stats_t;
+
+int scape_mask_stats(scape_handle* h, scape_mask_stats_t* out);
+
 /* ---- Dense AdamS baseline --------------------------------------------------
  * The comparator of the SCAPE pages ("3.26x speedup per step compared to
  * dense AdamS": abstract; gist.science technical summary §4): dense data

@@ -12,7 +12,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libscape.so")
-SOURCES = ["scape_api.cu", "k_fused.cu", "k_select.cu", "k_dense.cu", "scape_noalloc.cu"]
+SOURCES = ["scape_api.cu", "k_fused.cu", "k_select.cu", "k_dense.cu", "k_maskops.cu",
+           "scape_noalloc.cu"]
 
 NVCC_FLAGS = [
     "-O3", "-std=c++17", "-gencode", "arch=compute_103a,code=sm_103a", "-lineinfo",

@@ -1,0 +1,51 @@
+// Word-wise operations on packed masks, used by the mask diagnostics:
+// OR-accumulation of per-worker masks and popcounts of (a & b).
+#include "scape_device.cuh"
+#include "scape_kernels.cuh"
+
+namespace scape {
+namespace {
+
+__global__ __launch_bounds__(256) void mask_or(uint32_t* __restrict__ acc,
+                                               const uint32_t* __restrict__ m, uint64_t n,
+                                               int first) {
+  const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+  for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride)
+    acc[i] = first ? m[i] : (acc[i] | m[i]);
+}
+
+__global__ __launch_bounds__(256) void mask_popcount(const uint32_t* __restrict__ a,
+                                                     const uint32_t* __restrict__ b, uint64_t n,
+                                                     unsigned long long* __restrict__ out) {
+  __shared__ uint32_t part[9];
+  const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+  uint32_t cnt = 0;
+  for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride)
+    cnt += __popc(b ? (a[i] & b[i]) : a[i]);
+  uint32_t total;
+  block_incl_scan<256>(cnt, part, &total);
+  if (threadIdx.x == 0 && total) atomicAdd(out, (unsigned long long)total);
+}
+
+unsigned grid_for(uint64_t n) {
+  uint64_t g = (n + 255) / 256;
+  const uint64_t cap = (uint64_t)num_sms() * 8;
+  if (g > cap) g = cap;
+  return (unsigned)(g ? g : 1);
+}
+
+}  // namespace
+
+cudaError_t launch_mask_or(uint32_t* acc, const uint32_t* m, uint64_t nwords, bool first,
+                           cudaStream_t s) {
+  mask_or<<<grid_for(nwords), 256, 0, s>>>(acc, m, nwords, first ? 1 : 0);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_mask_popcount(const uint32_t* a, const uint32_t* b, uint64_t nwords,
+                                 unsigned long long* out, cudaStream_t s) {
+  mask_popcount<<<grid_for(nwords), 256, 0, s>>>(a, b, nwords, out);
+  return cudaGetLastError();
+}
+
+}  // namespace scape

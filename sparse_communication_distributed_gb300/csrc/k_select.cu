@@ -135,7 +135,7 @@ __device__ void select_one(const SelectArgs& p, SelectSmem& sm, const uint64_t c
   const uint64_t c0 = c * p.C;
   const uint32_t L = (uint32_t)((p.N - c0) < p.C ? (p.N - c0) : p.C);
   const uint32_t k = (c == p.n_ch - 1) ? p.k_last : p.k_full;
-  const int w = (int)(c / p.q);
+  const int w = p.rank_worker > 0 ? p.rank_worker - 1 : (int)(c / p.q);
   const uint32_t nwc = (L + 31) / 32;
   uint32_t* mout = p.mout + c0 / 32;
   const uint64_t base_c = c * (uint64_t)p.k_full;

@@ -47,6 +47,7 @@ struct scape_handle {
   uint32_t* fallback = nullptr;    // per chunk, see k_fused.cu
   uint32_t* n_fallback = nullptr;  // chunks redone by the standalone select (running total)
   uint16_t* stage = nullptr;  // scape_step_host staging, W x N bf16
+  uint32_t* diag = nullptr;   // scape_mask_stats: two masks + 3 counters (first use)
   int prev = 0;               // mask[prev] = M_{t-1} for the next step
   bool has_mask = false;      // a mask exists (built by a step or loaded)
   bool stepped = false;       // compact buffers hold a step's output
@@ -91,7 +92,7 @@ cudaError_t dalloc(scape_handle* h, T** p, uint64_t count) {
 
 void release(scape_handle* h) {
   void* ps[] = {h->theta, h->v, h->u, h->e, h->vals, h->bbar, h->idx, h->mask[0], h->mask[1],
-                h->fallback, h->n_fallback, h->stage};
+                h->fallback, h->n_fallback, h->stage, h->diag};
   for (void* p : ps)
     if (p) cudaFree(p);
   for (cudaEvent_t ev : h->ev_pool) cudaEventDestroy(ev);
@@ -552,5 +553,68 @@ SCAPE_API int scape_profile_read(scape_handle* h, double* ms, uint32_t* launches
     h->ev_pool.push_back(r.second.second);
   }
   h->ev_rec.clear();
+  return SCAPE_OK;
+}
+
+SCAPE_API int scape_mask_stats(scape_handle* h, scape_mask_stats_t* out) {
+  if (!h) return SCAPE_EINVAL;
+  if (!out) return fail(h, SCAPE_EINVAL, "out is NULL");
+  if (!h->stepped) return fail(h, SCAPE_ESTATE, "no step has run");
+  cudaError_t e = wait_last(h);
+  if (e != cudaSuccess) return cuda_fail(h, e, "scape_mask_stats");
+  const uint64_t nw = h->mask_alloc;
+  if (!h->diag) {
+    const uint64_t bytes = (2 * nw + 8) * sizeof(uint32_t);
+    if ((e = cudaMalloc(&h->diag, bytes)) != cudaSuccess) {
+      h->diag = nullptr;
+      cudaGetLastError();
+      return fail(h, e == cudaErrorMemoryAllocation ? SCAPE_ENOMEM : SCAPE_ECUDA,
+                  "diagnostics allocation failed: %s", cudaGetErrorString(e));
+    }
+    h->device_bytes += bytes;
+    if ((e = cudaMemset(h->diag, 0, bytes)) != cudaSuccess) return cuda_fail(h, e, "memset");
+  }
+  uint32_t* tmp = h->diag;
+  uint32_t* uni = h->diag + nw;
+  unsigned long long* cnt = reinterpret_cast<unsigned long long*>(h->diag + 2 * nw);
+  cudaStream_t s = h->last_stream;
+  const uint32_t* m_new = h->mask[h->prev];       // M_t, built by the last step
+  const uint32_t* m_used = h->mask[1 - h->prev];  // M_{t-1}, applied in the last step
+  if ((e = cudaMemsetAsync(cnt, 0, 3 * sizeof(unsigned long long), s)) != cudaSuccess)
+    return cuda_fail(h, e, "memset");
+  SelectArgs sa{};
+  sa.e = h->e;
+  sa.u = h->u;
+  sa.vals = h->vals;
+  sa.mprev = m_used;
+  sa.b1 = h->b1;
+  sa.c1 = h->c1;
+  sa.N = h->N;
+  sa.Np = h->Np;
+  sa.Kp = h->Kp;
+  sa.n_ch = h->n_ch;
+  sa.q = h->q;
+  sa.C = h->C;
+  sa.k_full = h->k_full;
+  sa.k_last = h->k_last;
+  sa.flags = nullptr;
+  sa.mout = tmp;
+  for (int w = 0; w < h->W; w++) {
+    sa.rank_worker = w + 1;
+    if ((e = launch_select(sa, false, s)) != cudaSuccess) return cuda_fail(h, e, "select");
+    if ((e = launch_mask_or(uni, tmp, nw, w == 0, s)) != cudaSuccess)
+      return cuda_fail(h, e, "mask_or");
+  }
+  if ((e = launch_mask_popcount(m_new, nullptr, nw, cnt, s)) != cudaSuccess ||
+      (e = launch_mask_popcount(m_new, m_used, nw, cnt + 1, s)) != cudaSuccess ||
+      (e = launch_mask_popcount(uni, nullptr, nw, cnt + 2, s)) != cudaSuccess)
+    return cuda_fail(h, e, "popcount");
+  unsigned long long host[3];
+  if ((e = cudaMemcpyAsync(host, cnt, sizeof host, cudaMemcpyDeviceToHost, s)) != cudaSuccess ||
+      (e = cudaStreamSynchronize(s)) != cudaSuccess)
+    return cuda_fail(h, e, "scape_mask_stats");
+  out->kept = host[0];
+  out->overlap_prev = host[1];
+  out->union_global_topk = host[2];
   return SCAPE_OK;
 }

@@ -50,6 +50,8 @@ struct SelectArgs {
   float b1, c1;
   uint32_t* mout;
   uint32_t* flags;  // NULL: every chunk; else only chunks with flags[c] != 0 (cleared)
+  int rank_worker;  // 0: each chunk ranks its owner's accumulator (the SCAPE rule);
+                    // w + 1: every chunk ranks worker w's (mask diagnostics)
   uint64_t N, Np, Kp, n_ch, q;
   uint32_t C, k_full, k_last;
 };
@@ -57,6 +59,12 @@ struct SelectArgs {
 // Launchers; all enqueue on "s" and return cudaGetLastError().
 cudaError_t launch_step_chunks(const FusedArgs& a, cudaStream_t s);
 cudaError_t launch_select(const SelectArgs& a, bool boot, cudaStream_t s);
+// acc = first ? m : (acc | m), over nwords words.
+cudaError_t launch_mask_or(uint32_t* acc, const uint32_t* m, uint64_t nwords, bool first,
+                           cudaStream_t s);
+// *out += popcount(a & b) (b may be NULL: popcount(a)), over nwords words.
+cudaError_t launch_mask_popcount(const uint32_t* a, const uint32_t* b, uint64_t nwords,
+                                 unsigned long long* out, cudaStream_t s);
 
 int num_sms();
 void set_thread_error(const char* msg);

@@ -23,7 +23,7 @@ PHASES = ("select_boot", "step", "select_fallback", "h2d")
 EXPORTS = ("scape_create", "scape_step", "scape_step_host", "scape_mask", "scape_destroy",
            "scape_info", "scape_read_state", "scape_load_state", "scape_read_sparse",
            "scape_last_error", "scape_profile", "scape_profile_read", "scape_step_noalloc",
-           "scape_dense_adams_step")
+           "scape_dense_adams_step", "scape_mask_stats")
 
 
 class ScapeError(RuntimeError):
@@ -87,6 +87,7 @@ def load_library(path: str = LIB_PATH):
     lib.scape_profile_read.argtypes = [vp, ctypes.POINTER(ctypes.c_double),
                                        ctypes.POINTER(ctypes.c_uint32)]
     lib.scape_step_noalloc.argtypes = [ctypes.POINTER(StepBuffers), ctypes.POINTER(vp), vp]
+    lib.scape_mask_stats.argtypes = [vp, ctypes.POINTER(ctypes.c_uint64 * 3)]
     f32 = ctypes.c_float
     lib.scape_dense_adams_step.argtypes = [vp, vp, vp, ctypes.POINTER(vp), i32, u64, f32, f32, f32,
                                            f32, f32, vp]
@@ -214,6 +215,12 @@ class Scape:
         self._check(self.lib.scape_read_sparse(self.h, w, idx.ctypes.data, vals.ctypes.data,
                                                offset, count, ctypes.byref(tot)))
         return idx, vals
+
+    def mask_stats(self) -> dict:
+        """kept, overlap_prev, union_global_topk of the last step (scape_mask_stats)."""
+        out = (ctypes.c_uint64 * 3)()
+        self._check(self.lib.scape_mask_stats(self.h, ctypes.byref(out)))
+        return {"kept": out[0], "overlap_prev": out[1], "union_global_topk": out[2]}
 
     def profile(self, enable: bool) -> None:
         self._check(self.lib.scape_profile(self.h, 1 if enable else 0))
