@@ -54,7 +54,8 @@ def load(path: str = SO):
     lib = ctypes.CDLL(path)
     lib.oracle_create.argtypes = [_u64p, ctypes.c_uint32, ctypes.c_uint32, ctypes.c_int,
                                   ctypes.c_double, ctypes.c_float, ctypes.c_float, ctypes.c_float,
-                                  ctypes.c_float, ctypes.c_float, _u64p, ctypes.c_uint64]
+                                  ctypes.c_float, ctypes.c_float, _u64p, ctypes.c_uint64,
+                                  ctypes.c_int]
     lib.oracle_create.restype = ctypes.c_void_p
     lib.oracle_destroy.argtypes = [ctypes.c_void_p]
     lib.oracle_domain_size.argtypes = [ctypes.c_void_p]
@@ -87,13 +88,15 @@ class Oracle:
     """One oracle instance over a domain of whole chunks (all chunks by default)."""
 
     def __init__(self, numel, chunk: int, W: int, density: float, beta1=0.9, beta2=0.95,
-                 lr=1e-3, wd=0.1, eps=1e-8, chunk_ids=None, lib_path: str = SO):
+                 lr=1e-3, wd=0.1, eps=1e-8, chunk_ids=None, lib_path: str = SO,
+                 per_tensor: bool = False):
         self.lib = load(lib_path)
         numel = np.ascontiguousarray(numel, dtype=np.uint64)
         ids = (np.zeros(0, np.uint64) if chunk_ids is None
                else np.ascontiguousarray(chunk_ids, dtype=np.uint64))
         self.h = self.lib.oracle_create(_p(numel, _u64p), numel.size, chunk, W, density, beta1,
-                                        beta2, lr, wd, eps, _p(ids, _u64p), ids.size)
+                                        beta2, lr, wd, eps, _p(ids, _u64p), ids.size,
+                                        1 if per_tensor else 0)
         if not self.h:
             raise ValueError("oracle_create rejected its arguments")
         self.W = W
@@ -109,9 +112,10 @@ class Oracle:
                                _p(self.chunk_k, _u32p), _p(self.chunk_owner, _i32p))
 
     @classmethod
-    def for_workload(cls, wl, density: float, chunk_ids=None, lib_path: str = SO):
+    def for_workload(cls, wl, density: float, chunk_ids=None, lib_path: str = SO,
+                     per_tensor: bool = False):
         return cls(wl.numel, wl.chunk, wl.W, density, wl.beta1, wl.beta2, wl.lr, wl.wd, wl.eps,
-                   chunk_ids=chunk_ids, lib_path=lib_path)
+                   chunk_ids=chunk_ids, lib_path=lib_path, per_tensor=per_tensor)
 
     def __del__(self):
         if getattr(self, "h", None):

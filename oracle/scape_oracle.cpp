@@ -37,8 +37,9 @@
  *   - top-k key: |a| as the fp32 bit pattern with the sign cleared, compared
  *     as an unsigned integer; k_c = floor(density * len_c) in IEEE double;
  *   - chunks of C coordinates tile the flat parameter vector, ignoring tensor
- *     boundaries; with n_ch chunks and q = ceil(n_ch/W), worker w owns chunks
- *     [w*q, min((w+1)*q, n_ch));
+ *     boundaries (or, in the per-tensor variant, tile each tensor separately,
+ *     the pages' "partitioned layers"); with n_ch chunks and q = ceil(n_ch/W),
+ *     worker w owns chunks [w*q, min((w+1)*q, n_ch));
  *   - step 0 has no earlier mask: M_{-1} is the selection (8) applied to the
  *     step-0 accumulators a_w = e_w + (b1*u_w + (1-b1)*g_w) before anything
  *     is written, so every step carries exactly k_c coordinates per chunk.
@@ -203,7 +204,7 @@ enum { OR_THETA = 0, OR_V = 1, OR_U = 2, OR_E = 3, OR_A = 4, OR_B = 5 };
  * domain; n_ids == 0 means every chunk.  Returns nullptr on bad arguments. */
 OR_API void* oracle_create(const uint64_t* numel, uint32_t n_tensors, uint32_t C, int W,
                            double density, float b1, float b2, float lr, float wd, float eps,
-                           const uint64_t* chunk_ids, uint64_t n_ids) {
+                           const uint64_t* chunk_ids, uint64_t n_ids, int per_tensor) {
   if (!numel || n_tensors == 0 || C == 0 || W < 1 || !(density > 0.0 && density <= 1.0))
     return nullptr;
   Oracle* o = new (std::nothrow) Oracle();
@@ -212,7 +213,19 @@ OR_API void* oracle_create(const uint64_t* numel, uint32_t n_tensors, uint32_t C
   if (o->N == 0) { delete o; return nullptr; }
   o->C = C; o->W = W; o->density = density;
   o->b1 = b1; o->b2 = b2; o->lr = lr; o->wd = wd; o->eps = eps;
-  o->n_chunks_total = (o->N + C - 1) / C;
+  // Chunk boundaries: every C coordinates of the flat vector, or (per_tensor)
+  // every C coordinates of each tensor, its last chunk shorter.
+  std::vector<uint64_t> cstart;
+  if (per_tensor) {
+    uint64_t off = 0;
+    for (uint32_t t = 0; t < n_tensors; t++) {
+      for (uint64_t x = 0; x < numel[t]; x += C) cstart.push_back(off + x);
+      off += numel[t];
+    }
+  } else {
+    for (uint64_t x = 0; x < o->N; x += C) cstart.push_back(x);
+  }
+  o->n_chunks_total = cstart.size();
   const uint64_t q = (o->n_chunks_total + W - 1) / W;
   std::vector<uint64_t> ids;
   if (n_ids == 0) {
@@ -228,8 +241,8 @@ OR_API void* oracle_create(const uint64_t* numel, uint32_t n_tensors, uint32_t C
   }
   for (uint64_t c : ids) {
     Chunk ch;
-    ch.start = c * (uint64_t)C;
-    uint64_t end = std::min<uint64_t>(ch.start + C, o->N);
+    ch.start = cstart[c];
+    uint64_t end = c + 1 < cstart.size() ? cstart[c + 1] : o->N;
     ch.len = (uint32_t)(end - ch.start);
     ch.k = (uint32_t)std::floor(density * (double)ch.len);
     ch.owner = (int)(c / q);

@@ -254,6 +254,31 @@ def pin_shard_geometry(lib: str = SO) -> None:
     assert int(o.chunk_k.astype(np.int64).sum()) == 104704
 
 
+def pin_per_tensor_chunks(lib: str = SO) -> None:
+    """Per-tensor chunking: every tensor is cut into ceil(n_t / C) chunks that
+    start at the tensor's offset, k_c = floor(density * len_c), shards stay
+    contiguous over the chunk list, and the top-k characterisation holds in
+    every such chunk (ties included)."""
+    numel = [96, 1000 * 32, 64, 3 * 1024 + 32, 32]
+    C, W, d = 1024, 3, 0.1
+    starts = np.concatenate([[0], np.cumsum(numel)])
+    expect = [int(starts[t]) + x for t, n in enumerate(numel) for x in range(0, n, C)]
+    wl = synth.Workload("pt", tuple((f"t{i}", (n,)) for i, n in enumerate(numel)), W=W, chunk=C,
+                        densities=(d,), steps=1, kind=synth.SYN_STUDENT_Q, sigma=2e-3, seed=6)
+    o = oracle.Oracle.for_workload(wl, d, lib_path=lib, per_tensor=True)
+    assert o.chunk_start.astype(np.int64).tolist() == expect
+    q = -(-len(expect) // W)
+    assert o.chunk_owner.tolist() == [j // q for j in range(len(expect))]
+    for t in range(3):
+        _run(o, wl, 1, t0=t)
+        m = o.mask(0)
+        for j in range(o.chunk_start.size):
+            s0, ln = int(o.chunk_start[j]), int(o.chunk_len[j])
+            k = math.floor(d * ln)
+            assert int(o.chunk_k[j]) == k
+            _check_topk_flags(o.get(oracle.A, int(o.chunk_owner[j]))[s0:s0 + ln], m[s0:s0 + ln], k)
+
+
 # -------------------------------------------------------------- off the mask
 
 def pin_offmask_decay(lib: str = SO) -> None:
@@ -339,7 +364,8 @@ def pin_dense_adams_constant_gradient(lib: str = SO) -> None:
 ALL_PINS = [
     pin_dense_adams, pin_single_worker_identity, pin_momentum_closed_form, pin_fixed_sum_order,
     pin_accumulator_split, pin_error_feedback_conservation, pin_delayed_mask,
-    pin_partitioned_topk, pin_topk_against_sort, pin_shard_geometry, pin_offmask_decay,
+    pin_partitioned_topk, pin_topk_against_sort, pin_shard_geometry, pin_per_tensor_chunks,
+    pin_offmask_decay,
     pin_dense_adams_single_worker, pin_dense_adams_matches_scape_density1,
     pin_dense_adams_constant_gradient,
 ]
