@@ -37,9 +37,7 @@ MUTANTS = [
     ("mask not delayed", "if (o.t == 0) {", "if (true) {"),
     ("bias correction added", "float q = bb / (std::sqrt(o.v[i]) + o.eps);",
      "float q = (bb / (1.0f - std::pow(o.b1, (float)(o.t + 1)))) / (std::sqrt(o.v[i]) + o.eps);"),
-    ("per-tensor chunks lose the tensor offset",
-     "for (uint64_t x = 0; x < numel[t]; x += C) cstart.push_back(off + x);",
-     "for (uint64_t x = 0; x < numel[t]; x += C) cstart.push_back(x + (t ? C : 0));"),
+    ("per-tensor chunks ignore tensor boundaries", "  if (per_tensor) {", "  if (false) {"),
     ("dense: mean misses 1/W", "const float gbar = s * invW;", "const float gbar = s;"),
     ("dense: second moment from the gradient", "v[i] = (b2 * v[i]) + (c2 * (m[i] * m[i]));",
      "v[i] = (b2 * v[i]) + (c2 * (gbar * gbar));"),
