@@ -51,6 +51,9 @@ def parse():
     ap.add_argument("--mask-stats", action="store_true",
                     help="report mask overlap and the fill-in of per-worker global top-k")
     ap.add_argument("--workers", type=int, default=None, help="override W of the workload")
+    ap.add_argument("--per-tensor", action="store_true", help="chunks restart at every tensor")
+    ap.add_argument("--residual-host", action="store_true",
+                    help="keep the residuals in page-locked host memory")
     return ap.parse_args()
 
 
@@ -228,7 +231,9 @@ def run_scape(args, wl, density):
     barrier = ranks.barrier
 
     N, W = wl.N, wl.W
-    sc = Scape.for_workload(wl, density)
+    from sparse_communication_distributed_gb300.scape import CHUNK_PER_TENSOR, RESIDUAL_HOST
+    flags = (CHUNK_PER_TENSOR if args.per_tensor else 0) | (RESIDUAL_HOST if args.residual_host else 0)
+    sc = Scape.for_workload(wl, density, flags=flags)
     K = sc.K
     th = torch.empty(N, dtype=torch.float32, device=dev)
     synth.gpu().theta_into(wl, th)
@@ -374,6 +379,8 @@ def run_scape(args, wl, density):
         "data": "synthetic",
         "config": {"workload": wl.name, "N": N, "W": W, "density": density, "chunk": wl.chunk,
                    "K": K, "grad_dtype": "bf16", "grad_batches": n_batches,
+                   "chunking": "per-tensor" if args.per_tensor else "flat",
+                   "residuals": "host (page-locked)" if args.residual_host else "HBM",
                    "parallelism": "replicas" if world > 1 else "single GPU, W emulated workers",
                    "l2": f"no flush: {sc.info['device_bytes'] / 1e9:.1f} GB resident state, "
                          "far larger than L2"},

@@ -82,6 +82,21 @@ enum {
   SCAPE_N_PHASES = 4
 };
 
+/* Options of scape_create_ex (bitwise OR). */
+enum {
+  /* Chunks tile every tensor separately ("partitioned layers", gist.science
+   * technical summary §2): tensor t is cut into ceil(numel_t / C) chunks, its
+   * last one shorter, k_c = floor(density * len_c) each.  Every tensor but the
+   * last must hold a multiple of 32 coordinates (chunks own whole mask words). */
+  SCAPE_CHUNK_PER_TENSOR = 1u,
+  /* The residuals e_w live in page-locked host memory (cudaHostAlloc, mapped)
+   * instead of HBM, read and written by the step kernel in place over the
+   * CPU-GPU link: W*N*4 bytes less device memory, at the link's bandwidth.
+   * The SCAPE pages offload residual buffers to CPU memory (technical summary
+   * §2 "Memory Optimization", §4). */
+  SCAPE_RESIDUAL_HOST = 2u
+};
+
 typedef struct {
   uint64_t N;          /* coordinates */
   uint32_t W;          /* emulated workers */
@@ -96,6 +111,8 @@ typedef struct {
   uint64_t device_bytes; /* device memory held by the handle */
   uint64_t select_fallbacks; /* chunks (over all steps) whose top-k the standalone select
                                 redid because their threshold bucket held too many ties */
+  uint32_t flags;      /* scape_create_ex options */
+  uint64_t host_bytes; /* page-locked host memory held (SCAPE_RESIDUAL_HOST) */
 } scape_info_t;
 
 /* Create a handle: computes the chunk/shard table, allocates all state on the
@@ -104,6 +121,12 @@ typedef struct {
  * On failure *out is NULL and nothing is leaked. */
 int scape_create(const scape_layout* layout, int W, double density, float beta1, float beta2,
                  float lr, float wd, float eps, scape_handle** out);
+
+/* scape_create with options (SCAPE_CHUNK_PER_TENSOR, SCAPE_RESIDUAL_HOST);
+ * flags = 0 is scape_create.  k_full and k_last of scape_info are then
+ * floor(density * C) and the last chunk's k. */
+int scape_create_ex(const scape_layout* layout, int W, double density, float beta1, float beta2,
+                    float lr, float wd, float eps, uint32_t flags, scape_handle** out);
 
 /* One optimizer step.  grad_ptrs: HOST array of W DEVICE pointers, each to N
  * bf16 gradients (16-byte aligned), borrowed read-only until the step has

@@ -66,6 +66,8 @@ def load(path: str = SO):
     lib.oracle_chunks.argtypes = [ctypes.c_void_p, _u64p, _u32p, _u32p, _i32p]
     lib.oracle_chunks.restype = ctypes.c_uint64
     lib.oracle_step.argtypes = [ctypes.c_void_p, _u16p]
+    lib.oracle_all_chunks.argtypes = [ctypes.c_void_p, _u64p, _u64p, _u64p]
+    lib.oracle_all_chunks.restype = ctypes.c_uint64
     lib.oracle_get.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, _f32p]
     lib.oracle_set.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, _f32p]
     lib.oracle_get_mask.argtypes = [ctypes.c_void_p, ctypes.c_int, _u8p]
@@ -110,6 +112,13 @@ class Oracle:
         self.chunk_owner = np.empty(nc, np.int32)
         self.lib.oracle_chunks(self.h, _p(self.chunk_start, _u64p), _p(self.chunk_len, _u32p),
                                _p(self.chunk_k, _u32p), _p(self.chunk_owner, _i32p))
+
+    def all_chunks(self):
+        """(start, len, k) of every chunk of the layout, as uint64 arrays."""
+        n = int(self.lib.oracle_all_chunks(self.h, None, None, None))
+        st, ln, k = (np.empty(n, np.uint64) for _ in range(3))
+        self.lib.oracle_all_chunks(self.h, _p(st, _u64p), _p(ln, _u64p), _p(k, _u64p))
+        return st, ln, k
 
     @classmethod
     def for_workload(cls, wl, density: float, chunk_ids=None, lib_path: str = SO,

@@ -78,6 +78,7 @@ struct Oracle {
   float b1 = 0, b2 = 0, lr = 0, wd = 0, eps = 0;
   uint64_t n_chunks_total = 0;
   std::vector<Chunk> chunks;          // the domain's chunks, ascending
+  std::vector<uint64_t> all_start, all_len, all_k;  // every chunk of the layout
   std::vector<uint64_t> dom_index;    // flat index of each domain position
   uint64_t n = 0;                     // domain size
 
@@ -226,6 +227,12 @@ OR_API void* oracle_create(const uint64_t* numel, uint32_t n_tensors, uint32_t C
     for (uint64_t x = 0; x < o->N; x += C) cstart.push_back(x);
   }
   o->n_chunks_total = cstart.size();
+  for (size_t c = 0; c < cstart.size(); c++) {
+    const uint64_t end = c + 1 < cstart.size() ? cstart[c + 1] : o->N;
+    o->all_start.push_back(cstart[c]);
+    o->all_len.push_back(end - cstart[c]);
+    o->all_k.push_back((uint64_t)std::floor(density * (double)(end - cstart[c])));
+  }
   const uint64_t q = (o->n_chunks_total + W - 1) / W;
   std::vector<uint64_t> ids;
   if (n_ids == 0) {
@@ -284,6 +291,18 @@ OR_API uint64_t oracle_chunks(void* h, uint64_t* start, uint32_t* len, uint32_t*
     if (owner) owner[j] = o->chunks[j].owner;
   }
   return o->chunks.size();
+}
+
+/* Every chunk of the layout (not only the domain): start, len, k. Returns the
+ * chunk count; any pointer may be NULL. */
+OR_API uint64_t oracle_all_chunks(void* h, uint64_t* start, uint64_t* len, uint64_t* k) {
+  Oracle* o = static_cast<Oracle*>(h);
+  for (size_t j = 0; j < o->all_start.size(); j++) {
+    if (start) start[j] = o->all_start[j];
+    if (len) len[j] = o->all_len[j];
+    if (k) k[j] = o->all_k[j];
+  }
+  return o->all_start.size();
 }
 
 /* One step; grads[W][n] are bf16 bit patterns over the domain. */

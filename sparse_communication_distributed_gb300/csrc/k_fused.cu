@@ -12,7 +12,9 @@
 //  0. load the chunk's words of M_{t-1} and their exclusive popcount prefix:
 //     the packed position of a kept coordinate i is
 //       base_c + popcount(M_{t-1} bits of the chunk before i),
-//     base_c = c * k_full (every earlier chunk keeps exactly k coordinates);
+//     base_c = c * k_full (every earlier chunk keeps exactly k coordinates),
+//     or the chunk table's base in the per-tensor variant, where chunks
+//     restart at every tensor (each tensor starts on a mask word);
 //  1. the owner's streaming pass (momentum, accumulate, mask select, residual,
 //     compaction into vals_owner), which also keeps every |a| as a 16-bit
 //     truncated key (fp32 bits 30..15) in shared memory and counts its top 12
@@ -413,11 +415,19 @@ __global__ __launch_bounds__(kNT, 1) void step_chunks(const FusedArgs p) {
   for (uint64_t c = blockIdx.x; c < p.n_ch; c += gridDim.x) {
     Chunk ch;
     ch.c = c;
-    ch.c0 = c * p.C;
-    ch.L = (uint32_t)((p.N - ch.c0) < p.C ? (p.N - ch.c0) : p.C);
-    ch.k = (c == p.n_ch - 1) ? p.k_last : p.k_full;
+    if (p.chunks) {
+      const ChunkDesc d = p.chunks[c];
+      ch.c0 = d.start;
+      ch.L = d.len;
+      ch.k = d.k;
+      ch.base = d.base;
+    } else {
+      ch.c0 = c * p.C;
+      ch.L = (uint32_t)((p.N - ch.c0) < p.C ? (p.N - ch.c0) : p.C);
+      ch.k = (c == p.n_ch - 1) ? p.k_last : p.k_full;
+      ch.base = c * (uint64_t)p.k_full;
+    }
     ch.nw = (ch.L + 31) / 32;
-    ch.base = c * (uint64_t)p.k_full;
     ch.owner = (int)(c / p.q);
 
     // phase 0: M_{t-1} words of the chunk, their popcount prefix; clear the histogram

@@ -132,13 +132,23 @@ __device__ __forceinline__ int quad_keys(const SelectArgs& p, const SelectSmem& 
 template <int SRC>
 __device__ void select_one(const SelectArgs& p, SelectSmem& sm, const uint64_t c) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const uint64_t c0 = c * p.C;
-  const uint32_t L = (uint32_t)((p.N - c0) < p.C ? (p.N - c0) : p.C);
-  const uint32_t k = (c == p.n_ch - 1) ? p.k_last : p.k_full;
+  uint64_t c0, base_c;
+  uint32_t L, k;
+  if (p.chunks) {
+    const ChunkDesc d = p.chunks[c];
+    c0 = d.start;
+    L = d.len;
+    k = d.k;
+    base_c = d.base;
+  } else {
+    c0 = c * p.C;
+    L = (uint32_t)((p.N - c0) < p.C ? (p.N - c0) : p.C);
+    k = (c == p.n_ch - 1) ? p.k_last : p.k_full;
+    base_c = c * (uint64_t)p.k_full;
+  }
   const int w = p.rank_worker > 0 ? p.rank_worker - 1 : (int)(c / p.q);
   const uint32_t nwc = (L + 31) / 32;
   uint32_t* mout = p.mout + c0 / 32;
-  const uint64_t base_c = c * (uint64_t)p.k_full;
 
   if (k == 0 || k == L) {
     for (uint32_t j = tid; j < nwc; j += kNT) {

@@ -48,6 +48,10 @@ struct scape_handle {
   uint32_t* n_fallback = nullptr;  // chunks redone by the standalone select (running total)
   uint16_t* stage = nullptr;  // scape_step_host staging, W x N bf16
   uint32_t* diag = nullptr;   // scape_mask_stats: two masks + 3 counters (first use)
+  uint32_t flags = 0;         // SCAPE_CHUNK_PER_TENSOR | SCAPE_RESIDUAL_HOST
+  std::vector<ChunkDesc> chunks;     // chunk table (host copy, every mode)
+  ChunkDesc* chunks_dev = nullptr;   // device copy, per-tensor mode only
+  uint64_t host_bytes = 0;           // page-locked host memory held (residuals)
   int prev = 0;               // mask[prev] = M_{t-1} for the next step
   bool has_mask = false;      // a mask exists (built by a step or loaded)
   bool stepped = false;       // compact buffers hold a step's output
@@ -91,10 +95,14 @@ cudaError_t dalloc(scape_handle* h, T** p, uint64_t count) {
 }
 
 void release(scape_handle* h) {
-  void* ps[] = {h->theta, h->v, h->u, h->e, h->vals, h->bbar, h->idx, h->mask[0], h->mask[1],
-                h->fallback, h->n_fallback, h->stage, h->diag};
+  void* ps[] = {h->theta, h->v, h->u, h->vals, h->bbar, h->idx, h->mask[0], h->mask[1],
+                h->fallback, h->n_fallback, h->stage, h->diag, h->chunks_dev};
   for (void* p : ps)
     if (p) cudaFree(p);
+  if (h->e) {
+    if (h->flags & SCAPE_RESIDUAL_HOST) cudaFreeHost(h->e);
+    else cudaFree(h->e);
+  }
   for (cudaEvent_t ev : h->ev_pool) cudaEventDestroy(ev);
   for (auto& r : h->ev_rec) {
     cudaEventDestroy(r.second.first);
@@ -145,15 +153,18 @@ cudaError_t wait_last(scape_handle* h) {
 // and none past N.
 bool mask_valid(const scape_handle* h, const std::vector<uint32_t>& m, std::string& why) {
   for (uint64_t c = 0; c < h->n_ch; c++) {
-    const uint64_t w0 = c * h->C / 32;
-    const uint64_t len = std::min<uint64_t>(h->C, h->N - c * h->C);
-    const uint64_t nw = (len + 31) / 32;
+    const ChunkDesc& d = h->chunks[c];
+    const uint64_t w0 = d.start / 32;
+    const uint64_t nw = (d.len + 31) / 32;
     uint64_t cnt = 0;
-    for (uint64_t j = 0; j < nw; j++) cnt += __builtin_popcount(m[w0 + j]);
-    const uint64_t k = c == h->n_ch - 1 ? h->k_last : h->k_full;
-    if (cnt != k) {
+    for (uint64_t j = 0; j < nw; j++) {
+      uint32_t word = m[w0 + j];
+      if (j == nw - 1 && (d.len & 31)) word &= (1u << (d.len & 31)) - 1u;
+      cnt += __builtin_popcount(word);
+    }
+    if (cnt != d.k) {
       why = "chunk " + std::to_string(c) + " has " + std::to_string(cnt) + " bits, needs " +
-            std::to_string(k);
+            std::to_string(d.k);
       return false;
     }
   }
@@ -174,8 +185,9 @@ namespace scape {
 void set_thread_error(const char* msg) { g_create_err = msg; }
 }  // namespace scape
 
-SCAPE_API int scape_create(const scape_layout* layout, int W, double density, float beta1,
-                           float beta2, float lr, float wd, float eps, scape_handle** out) {
+SCAPE_API int scape_create_ex(const scape_layout* layout, int W, double density, float beta1,
+                              float beta2, float lr, float wd, float eps, uint32_t flags,
+                              scape_handle** out) {
   if (!out) return fail(nullptr, SCAPE_EINVAL, "out is NULL");
   *out = nullptr;
   if (!layout || !layout->numel || layout->n_tensors == 0)
@@ -197,6 +209,14 @@ SCAPE_API int scape_create(const scape_layout* layout, int W, double density, fl
   if (!std::isfinite(beta1) || !std::isfinite(beta2) || !std::isfinite(lr) ||
       !std::isfinite(wd) || !(eps > 0.0f) || !std::isfinite(eps))
     return fail(nullptr, SCAPE_EINVAL, "hyper-parameters must be finite and eps > 0");
+  if (flags & ~(uint32_t)(SCAPE_CHUNK_PER_TENSOR | SCAPE_RESIDUAL_HOST))
+    return fail(nullptr, SCAPE_EINVAL, "unknown flags 0x%x", flags);
+  if (flags & SCAPE_CHUNK_PER_TENSOR)
+    for (uint32_t i = 0; i + 1 < layout->n_tensors; i++)
+      if (layout->numel[i] % 32)
+        return fail(nullptr, SCAPE_EINVAL,
+                    "per-tensor chunks need every tensor but the last to hold a multiple of 32 "
+                    "coordinates (tensor %u has %llu)", i, (unsigned long long)layout->numel[i]);
 
   scape_handle* h = new (std::nothrow) scape_handle();
   if (!h) return fail(nullptr, SCAPE_ENOMEM, "host allocation failed");
@@ -211,19 +231,60 @@ SCAPE_API int scape_create(const scape_layout* layout, int W, double density, fl
   h->Np = (N + kTile - 1) / kTile * kTile;
   h->mask_words = (N + 31) / 32;
   h->mask_alloc = h->Np / 32;
-  h->n_ch = (N + C - 1) / C;
+  h->flags = flags;
+  // chunk table: every C coordinates of the flat vector, or of each tensor
+  {
+    uint64_t off = 0, base = 0;
+    auto add = [&](uint64_t start, uint64_t len) {
+      ChunkDesc d;
+      d.start = start;
+      d.len = (uint32_t)len;
+      d.k = (uint32_t)std::floor(density * (double)len);
+      d.base = base;
+      base += d.k;
+      h->chunks.push_back(d);
+    };
+    if (flags & SCAPE_CHUNK_PER_TENSOR) {
+      for (uint32_t t = 0; t < layout->n_tensors; t++) {
+        for (uint64_t x = 0; x < layout->numel[t]; x += C)
+          add(off + x, std::min<uint64_t>(C, layout->numel[t] - x));
+        off += layout->numel[t];
+      }
+    } else {
+      for (uint64_t x = 0; x < N; x += C) add(x, std::min<uint64_t>(C, N - x));
+    }
+    h->K = base;
+  }
+  h->n_ch = h->chunks.size();
   h->q = (h->n_ch + W - 1) / W;
   h->k_full = (uint32_t)std::floor(density * (double)C);
-  const uint64_t last_len = N - (h->n_ch - 1) * C;
-  h->k_last = (uint32_t)std::floor(density * (double)last_len);
-  h->K = (h->n_ch - 1) * (uint64_t)h->k_full + h->k_last;
+  h->k_last = h->chunks.back().k;
   h->Kp = (h->K + 3) / 4 * 4;
 
   cudaError_t e = cudaSuccess;
   if (e == cudaSuccess) e = dalloc(h, &h->theta, h->Np);
   if (e == cudaSuccess) e = dalloc(h, &h->v, h->Np);
   if (e == cudaSuccess) e = dalloc(h, &h->u, (uint64_t)W * h->Np);
-  if (e == cudaSuccess) e = dalloc(h, &h->e, (uint64_t)W * h->Np);
+  if (flags & SCAPE_RESIDUAL_HOST) {
+    // residuals in page-locked host memory, read and written by the step
+    // kernel in place over the CPU-GPU link
+    const uint64_t bytes = (uint64_t)W * h->Np * sizeof(float);
+    void* hp = nullptr;
+    if (e == cudaSuccess) e = cudaHostAlloc(&hp, bytes, cudaHostAllocMapped);
+    if (e == cudaSuccess) {
+      void* dp = nullptr;
+      std::memset(hp, 0, bytes);
+      e = cudaHostGetDevicePointer(&dp, hp, 0);
+      if (e == cudaSuccess) {
+        h->e = static_cast<float*>(dp);
+        h->host_bytes += bytes;
+      } else {
+        cudaFreeHost(hp);
+      }
+    }
+  } else if (e == cudaSuccess) {
+    e = dalloc(h, &h->e, (uint64_t)W * h->Np);
+  }
   if (e == cudaSuccess) e = dalloc(h, &h->vals, (uint64_t)W * h->Kp);
   if (e == cudaSuccess) e = dalloc(h, &h->bbar, h->Kp);
   if (e == cudaSuccess) e = dalloc(h, &h->idx, h->Kp);
@@ -231,6 +292,12 @@ SCAPE_API int scape_create(const scape_layout* layout, int W, double density, fl
   if (e == cudaSuccess) e = dalloc(h, &h->mask[1], h->mask_alloc);
   if (e == cudaSuccess) e = dalloc(h, &h->fallback, h->n_ch);
   if (e == cudaSuccess) e = dalloc(h, &h->n_fallback, 1);
+  if (e == cudaSuccess && (flags & SCAPE_CHUNK_PER_TENSOR)) {
+    e = dalloc(h, &h->chunks_dev, h->n_ch);
+    if (e == cudaSuccess)
+      e = cudaMemcpy(h->chunks_dev, h->chunks.data(), h->n_ch * sizeof(ChunkDesc),
+                     cudaMemcpyHostToDevice);
+  }
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {
     const int code = (e == cudaErrorMemoryAllocation) ? SCAPE_ENOMEM : SCAPE_ECUDA;
@@ -243,6 +310,11 @@ SCAPE_API int scape_create(const scape_layout* layout, int W, double density, fl
   }
   *out = h;
   return SCAPE_OK;
+}
+
+SCAPE_API int scape_create(const scape_layout* layout, int W, double density, float beta1,
+                           float beta2, float lr, float wd, float eps, scape_handle** out) {
+  return scape_create_ex(layout, W, density, beta1, beta2, lr, wd, eps, 0u, out);
 }
 
 SCAPE_API void scape_destroy(scape_handle* h) {
@@ -275,6 +347,8 @@ SCAPE_API int scape_info(const scape_handle* h, scape_info_t* out) {
       cudaMemcpy(&nf, h->n_fallback, 4, cudaMemcpyDeviceToHost) != cudaSuccess)
     return cuda_fail(hm, cudaGetLastError(), "scape_info");
   out->select_fallbacks = nf;
+  out->flags = h->flags;
+  out->host_bytes = h->host_bytes;
   return SCAPE_OK;
 }
 
@@ -298,6 +372,7 @@ static int step_device(scape_handle* h, const uint16_t* const* g, cudaStream_t s
   sa.C = h->C;
   sa.k_full = h->k_full;
   sa.k_last = h->k_last;
+  sa.chunks = h->chunks_dev;
 
   if (!h->has_mask) {  // step 0: M_{-1} from the step-0 accumulators
     PhaseTimer pt(h, SCAPE_PH_SELECT_BOOT, s);
@@ -321,6 +396,7 @@ static int step_device(scape_handle* h, const uint16_t* const* g, cudaStream_t s
     a.mout = mcur;
     a.fallback = h->fallback;
     a.n_fallback = h->n_fallback;
+    a.chunks = h->chunks_dev;
     a.N = h->N;
     a.Np = h->Np;
     a.Kp = h->Kp;
@@ -598,6 +674,7 @@ SCAPE_API int scape_mask_stats(scape_handle* h, scape_mask_stats_t* out) {
   sa.k_full = h->k_full;
   sa.k_last = h->k_last;
   sa.flags = nullptr;
+  sa.chunks = h->chunks_dev;
   sa.mout = tmp;
   for (int w = 0; w < h->W; w++) {
     sa.rank_worker = w + 1;

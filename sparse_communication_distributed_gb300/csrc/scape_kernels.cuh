@@ -20,6 +20,14 @@ constexpr int kMaxW = 64;
 constexpr int kTile = 256;             // coordinates per warp tile (8 per thread)
 constexpr uint32_t kMaxChunk = 65536;  // largest chunk (16-bit in-chunk index)
 
+// One chunk of the per-tensor variant (chunks restart at every tensor).
+struct ChunkDesc {
+  uint64_t start;  // first coordinate (a multiple of 32)
+  uint64_t base;   // packed position of its first kept value
+  uint32_t len;    // coordinates
+  uint32_t k;      // kept coordinates
+};
+
 struct FusedArgs {
   const uint16_t* grads[kMaxW];
   float* u;
@@ -33,6 +41,7 @@ struct FusedArgs {
   uint32_t* mout;
   uint32_t* fallback;    // per chunk: 1 = selection left to the standalone select
   uint32_t* n_fallback;  // count of such chunks (diagnostic)
+  const ChunkDesc* chunks;  // NULL: chunk c = [c*C, c*C + C) of the flat vector
   uint64_t N, Np, Kp, n_ch, q;
   uint32_t C, k_full, k_last;
   int W;
@@ -52,6 +61,7 @@ struct SelectArgs {
   uint32_t* flags;  // NULL: every chunk; else only chunks with flags[c] != 0 (cleared)
   int rank_worker;  // 0: each chunk ranks its owner's accumulator (the SCAPE rule);
                     // w + 1: every chunk ranks worker w's (mask diagnostics)
+  const ChunkDesc* chunks;  // NULL: chunk c = [c*C, c*C + C) of the flat vector
   uint64_t N, Np, Kp, n_ch, q;
   uint32_t C, k_full, k_last;
 };

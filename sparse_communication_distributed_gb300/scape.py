@@ -20,7 +20,8 @@ THETA, V, U, E, MASK, STEP = 0, 1, 2, 3, 4, 5
 PHASES = ("select_boot", "step", "select_fallback", "h2d")
 
 # Symbols declared in include/scape.h (checked by the ABI test).
-EXPORTS = ("scape_create", "scape_step", "scape_step_host", "scape_mask", "scape_destroy",
+CHUNK_PER_TENSOR, RESIDUAL_HOST = 1, 2
+EXPORTS = ("scape_create", "scape_create_ex", "scape_step", "scape_step_host", "scape_mask", "scape_destroy",
            "scape_info", "scape_read_state", "scape_load_state", "scape_read_sparse",
            "scape_last_error", "scape_profile", "scape_profile_read", "scape_step_noalloc",
            "scape_dense_adams_step", "scape_mask_stats")
@@ -42,7 +43,8 @@ class _Info(ctypes.Structure):
                 ("n_chunks", ctypes.c_uint64), ("chunks_per_worker", ctypes.c_uint64),
                 ("k_full", ctypes.c_uint32), ("k_last", ctypes.c_uint32), ("K", ctypes.c_uint64),
                 ("mask_words", ctypes.c_uint64), ("step", ctypes.c_int64),
-                ("device_bytes", ctypes.c_uint64), ("select_fallbacks", ctypes.c_uint64)]
+                ("device_bytes", ctypes.c_uint64), ("select_fallbacks", ctypes.c_uint64),
+                ("flags", ctypes.c_uint32), ("host_bytes", ctypes.c_uint64)]
 
 
 class StepBuffers(ctypes.Structure):
@@ -72,6 +74,9 @@ def load_library(path: str = LIB_PATH):
     lib.scape_create.argtypes = [ctypes.POINTER(_Layout), i32, ctypes.c_double, ctypes.c_float,
                                  ctypes.c_float, ctypes.c_float, ctypes.c_float, ctypes.c_float,
                                  ctypes.POINTER(vp)]
+    lib.scape_create_ex.argtypes = [ctypes.POINTER(_Layout), i32, ctypes.c_double,
+                                    ctypes.c_float, ctypes.c_float, ctypes.c_float, ctypes.c_float,
+                                    ctypes.c_float, ctypes.c_uint32, ctypes.POINTER(vp)]
     lib.scape_step.argtypes = [vp, ctypes.POINTER(vp), vp]
     lib.scape_step_host.argtypes = [vp, ctypes.POINTER(vp), vp]
     lib.scape_mask.argtypes = [vp, vp]
@@ -115,21 +120,23 @@ class Scape:
     """One SCAPE optimizer instance (a libscape handle)."""
 
     def __init__(self, numel, chunk: int, W: int, density: float, beta1: float = 0.9,
-                 beta2: float = 0.95, lr: float = 1e-3, wd: float = 0.1, eps: float = 1e-8):
+                 beta2: float = 0.95, lr: float = 1e-3, wd: float = 0.1, eps: float = 1e-8,
+                 flags: int = 0):
         self.lib = load_library()
         arr = np.ascontiguousarray(numel, dtype=np.uint64)
         lay = _Layout(arr.size, arr.ctypes.data_as(ctypes.POINTER(ctypes.c_uint64)), chunk)
         h = ctypes.c_void_p()
-        rc = self.lib.scape_create(ctypes.byref(lay), W, density, beta1, beta2, lr, wd, eps,
-                                   ctypes.byref(h))
+        rc = self.lib.scape_create_ex(ctypes.byref(lay), W, density, beta1, beta2, lr, wd, eps,
+                                      flags, ctypes.byref(h))
         if rc != SCAPE_OK:
             raise ScapeError(rc, self.lib.scape_last_error(None).decode())
         self.h = h
         self.info = self._info()
 
     @classmethod
-    def for_workload(cls, wl, density: float) -> "Scape":
-        return cls(wl.numel, wl.chunk, wl.W, density, wl.beta1, wl.beta2, wl.lr, wl.wd, wl.eps)
+    def for_workload(cls, wl, density: float, flags: int = 0) -> "Scape":
+        return cls(wl.numel, wl.chunk, wl.W, density, wl.beta1, wl.beta2, wl.lr, wl.wd, wl.eps,
+                   flags=flags)
 
     def _check(self, rc: int) -> None:
         if rc != SCAPE_OK:

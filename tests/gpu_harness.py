@@ -39,9 +39,9 @@ def assert_close_exact(name: str, got: np.ndarray, ref: np.ndarray) -> None:
 class GpuRun:
     """libscape on a workload, inputs from the GPU build of the generator."""
 
-    def __init__(self, wl, density: float, theta0: bool = True):
+    def __init__(self, wl, density: float, theta0: bool = True, flags: int = 0):
         self.wl = wl
-        self.sc = Scape.for_workload(wl, density)
+        self.sc = Scape.for_workload(wl, density, flags=flags)
         self.dev = torch.device("cuda")
         self.grads = [torch.empty(wl.N, dtype=torch.int16, device=self.dev) for _ in range(wl.W)]
         if theta0:
@@ -72,9 +72,11 @@ class OracleRun:
     """The oracle over a set of whole chunks, inputs from the CPU build of the
     generator."""
 
-    def __init__(self, wl, density: float, chunk_ids=None, theta0: bool = True):
+    def __init__(self, wl, density: float, chunk_ids=None, theta0: bool = True,
+                 per_tensor: bool = False):
         self.wl = wl
-        self.o = oracle.Oracle.for_workload(wl, density, chunk_ids=chunk_ids)
+        self.o = oracle.Oracle.for_workload(wl, density, chunk_ids=chunk_ids,
+                                            per_tensor=per_tensor)
         if theta0:
             self.o.set(oracle.THETA, synth.cpu().theta0(wl, self.o.index))
         self.t = 0
@@ -91,13 +93,14 @@ class OracleRun:
 def compare(g: GpuRun, r: OracleRun, what: str = "") -> None:
     """Compare the GPU state with the oracle over the oracle's chunks."""
     o, sc, W = r.o, g.sc, g.wl.W
-    info = sc.info
     m_gen = o.mask(0)
     m_used = o.mask(1)
+    all_start, _, all_k = o.all_chunks()
+    all_base = np.concatenate([[0], np.cumsum(all_k.astype(np.int64))])
     pos = 0
     for j in range(o.chunk_start.size):
         s, ln, k = int(o.chunk_start[j]), int(o.chunk_len[j]), int(o.chunk_k[j])
-        c = s // g.wl.chunk
+        c = int(np.searchsorted(all_start, s))
         sl = slice(pos, pos + ln)
         tag = f"{what} chunk {c}"
         assert_close_exact(f"theta {tag}", sc.read(THETA, offset=s, count=ln), o.get(oracle.THETA)[sl])
@@ -114,8 +117,8 @@ def compare(g: GpuRun, r: OracleRun, what: str = "") -> None:
         if not np.array_equal(words, ref):
             bad = np.nonzero(words != ref)[0]
             raise AssertionError(f"mask {tag}: {bad.size} words differ, first word {bad[0]}")
-        # compact buffers of this chunk: K positions [c*k_full, c*k_full + k)
-        base = c * info["k_full"]
+        # compact buffers of this chunk: packed positions [base_c, base_c + k)
+        base = int(all_base[c])
         kept_local = np.nonzero(m_used[sl])[0]
         assert kept_local.size == k, (tag, kept_local.size, k)
         if k:
@@ -145,10 +148,11 @@ def sample_chunks(wl, n_extra: int = 4, seed: int = 0) -> list[int]:
 _POPC8 = np.array([bin(i).count("1") for i in range(256)], np.uint8)
 
 
-def check_full_mask(g: GpuRun) -> None:
+def check_full_mask(g: GpuRun, r: OracleRun | None = None) -> None:
     """Properties over the full size: every chunk of the next mask carries
     exactly k_c bits, none past N; the last step's coordinate list is strictly
-    increasing and has K entries."""
+    increasing and has K entries.  Chunk boundaries come from the oracle's
+    layout table when given (per-tensor chunks), else from C."""
     sc, wl = g.sc, g.wl
     info = sc.info
     words = sc.mask()
@@ -157,10 +161,20 @@ def check_full_mask(g: GpuRun) -> None:
     if N % 32:
         assert (int(words[-1]) >> (N % 32)) == 0, "bits past N"
     per_byte = _POPC8[words.view(np.uint8)]
-    full = (per_byte[: (nch - 1) * (C // 8)].reshape(nch - 1, C // 8).sum(axis=1, dtype=np.int64)
-            if nch > 1 else np.zeros(0))
-    assert np.all(full == info["k_full"]), "a full chunk with the wrong bit count"
-    assert int(per_byte[(nch - 1) * (C // 8):].sum(dtype=np.int64)) == info["k_last"]
+    if r is not None:
+        st, ln, k = r.o.all_chunks()
+        assert st.size == nch
+        cum = np.concatenate([[0], np.cumsum(per_byte, dtype=np.int64)])
+        # chunk starts are multiples of 32, so chunk bit counts are byte sums
+        # except a ragged last chunk, which ends at N (no bits past it)
+        ends = np.minimum((st + ln + 7) // 8, per_byte.size).astype(np.int64)
+        counts = cum[ends] - cum[(st // 8).astype(np.int64)]
+        assert np.array_equal(counts, k.astype(np.int64)), "a chunk with the wrong bit count"
+    else:
+        full = (per_byte[: (nch - 1) * (C // 8)].reshape(nch - 1, C // 8).sum(axis=1, dtype=np.int64)
+                if nch > 1 else np.zeros(0))
+        assert np.all(full == info["k_full"]), "a full chunk with the wrong bit count"
+        assert int(per_byte[(nch - 1) * (C // 8):].sum(dtype=np.int64)) == info["k_last"]
     idx, _ = sc.sparse(-1)
     assert idx.size == info["K"]
     assert np.all(np.diff(idx.astype(np.int64)) > 0)

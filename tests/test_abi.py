@@ -78,3 +78,16 @@ def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     with pytest.raises(ImportError):
         scape.load_library(str(tmp_path / "missing.so"))
     assert pkg.Scape is scape.Scape
+
+
+def test_create_ex_rejects_bad_flags(lib):
+    arr = np.asarray([100, 64], np.uint64)
+    lay = scape._Layout(arr.size, arr.ctypes.data_as(ctypes.POINTER(ctypes.c_uint64)), 64)
+    h = ctypes.c_void_p()
+    assert lib.scape_create_ex(ctypes.byref(lay), 2, 0.1, 0.9, 0.95, 1e-3, 0.1, 1e-8, 8,
+                               ctypes.byref(h)) == scape.SCAPE_EINVAL
+    assert "unknown flags" in lib.scape_last_error(None).decode()
+    # per-tensor chunks: a tensor before the last that is not a multiple of 32
+    assert lib.scape_create_ex(ctypes.byref(lay), 2, 0.1, 0.9, 0.95, 1e-3, 0.1, 1e-8,
+                               scape.CHUNK_PER_TENSOR, ctypes.byref(h)) == scape.SCAPE_EINVAL
+    assert "multiple of 32" in lib.scape_last_error(None).decode()

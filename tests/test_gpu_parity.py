@@ -218,3 +218,57 @@ def test_full_size_sampled_chunks(name, density):
     wl = synth.WORKLOADS[name]
     ids = sample_chunks(wl)
     _run_both(wl, density, wl.steps, chunk_ids=ids)
+
+
+# ---- variants: per-tensor chunks, residuals in host memory ---------------------------
+
+from sparse_communication_distributed_gb300.scape import CHUNK_PER_TENSOR, RESIDUAL_HOST  # noqa: E402
+
+
+def _per_tensor_run(wl, density, steps, chunk_ids=None):
+    g = GpuRun(wl, density, flags=CHUNK_PER_TENSOR)
+    r = OracleRun(wl, density, chunk_ids=chunk_ids, per_tensor=True)
+    try:
+        assert g.sc.info["n_chunks"] == r.o.all_chunks()[0].size
+        assert g.sc.K == int(r.o.all_chunks()[2].astype(np.int64).sum())
+        for t in range(steps):
+            g.step()
+            r.step()
+            compare(g, r, f"step {t}")
+        check_full_mask(g, r)
+    finally:
+        g.close()
+
+
+def test_per_tensor_chunks_small():
+    # tensors of 96 .. 32000 coordinates (the last one ragged) cut separately
+    numel = [96, 32000, 64, 3104, 1024, 4096 + 33]
+    wl = synth.Workload("per-tensor", tuple((f"t{i}", (n,)) for i, n in enumerate(numel)), W=3,
+                        chunk=1024, densities=(0.1,), steps=4, kind=synth.SYN_STUDENT_Q,
+                        sigma=1e-3, seed=60)
+    _per_tensor_run(wl, 0.1, 4)
+
+
+def test_per_tensor_gpt2_full_size_sampled():
+    wl = synth.WORKLOADS["gpt2-medium-w8"]
+    probe = oracle.Oracle.for_workload(wl, 0.01, chunk_ids=[0], per_tensor=True)
+    nch = probe.all_chunks()[0].size
+    q = -(-nch // wl.W)
+    ids = {0, 1, 2, nch - 2, nch - 1}
+    for w in range(1, wl.W):
+        ids |= {w * q - 1, w * q}
+    ids |= set(int(x) for x in np.random.default_rng(1).integers(0, nch, 4))
+    _per_tensor_run(wl, 0.01, 4, chunk_ids=sorted(ids))
+
+
+def test_residuals_in_host_memory():
+    wl = synth.tiny(3 * 4096 + 200, 3, 4096, 0.05, seed=61)
+    g, r = GpuRun(wl, 0.05, flags=RESIDUAL_HOST), OracleRun(wl, 0.05)
+    try:
+        assert g.sc.info["host_bytes"] >= 3 * wl.N * 4
+        for t in range(3):
+            g.step()
+            r.step()
+            compare(g, r, f"step {t}")
+    finally:
+        g.close()
