@@ -343,6 +343,38 @@ __device__ bool select_chunk(const FusedArgs& p, const Shared& sh, const Chunk& 
   return true;
 }
 
+// vals_0[r] + vals_1[r] + ... + vals_{W-1}[r], added left to right.  The loads
+// of each group of 8 workers are issued before any of them is added, so their
+// memory latencies overlap instead of queueing one after another.
+__device__ __forceinline__ float ordered_sum(const FusedArgs& p, uint32_t r) {
+  const float* v = p.vals + r;
+  float s = 0.0f;
+  for (int w0 = 0; w0 < p.W; w0 += 8) {
+    float x[8];
+#pragma unroll
+    for (int j = 0; j < 8; j++) x[j] = (w0 + j < p.W) ? v[(uint64_t)(w0 + j) * p.Kp] : 0.0f;
+#pragma unroll
+    for (int j = 0; j < 8; j++)
+      if (w0 + j < p.W) s = (w0 + j == 0) ? x[j] : s + x[j];
+  }
+  return s;
+}
+
+__device__ __forceinline__ void prefetch_l2(const void* q) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(q));
+}
+
+// Before a barrier: ask L2 for this thread's first tile of the next phase, so
+// the memory pipe does not run dry while the CTA waits and restarts.
+__device__ __forceinline__ void prefetch_worker_tile(const FusedArgs& p, uint64_t c0, uint32_t L,
+                                                     int w) {
+  const uint32_t i0 = (threadIdx.x >> 5) * 256 + (threadIdx.x & 31) * 8;
+  if (i0 + 8 > L) return;
+  prefetch_l2(p.grads[w] + c0 + i0);
+  prefetch_l2(p.u + (uint64_t)w * p.Np + c0 + i0);
+  prefetch_l2(p.e + (uint64_t)w * p.Np + c0 + i0);
+}
+
 // Phase 4: fixed-order W-way sum of the compact buffers and the AdamS update.
 __device__ __forceinline__ void update_chunk(const FusedArgs& p, const Shared& sh,
                                              const Chunk& ch) {
@@ -382,9 +414,7 @@ __device__ __forceinline__ void update_chunk(const FusedArgs& p, const Shared& s
       float bb = 0.0f;
       if (m) {
         const uint32_t r = rank0 + __popc(byte & ((1u << jj) - 1u));
-        float s = p.vals[r];
-        for (int w = 1; w < p.W; w++) s = s + p.vals[(uint64_t)w * p.Kp + r];
-        bb = s * invW;
+        bb = ordered_sum(p, r) * invW;
         p.bbar[r] = bb;
         p.idx[r] = (uint32_t)(ch.c0 + i0 + jj);
       }
@@ -451,6 +481,7 @@ __global__ __launch_bounds__(kNT, 1) void step_chunks(const FusedArgs p) {
 
     // phase 1: the owner's pass, keeping its keys
     stream_worker<true>(p, sh, ch, ch.owner);
+    if (p.W > 1) prefetch_worker_tile(p, ch.c0, ch.L, ch.owner == 0 ? 1 : 0);
     __syncthreads();
 
     // phase 2: top-k of the owner's |a| -> mask words of M_t
@@ -466,10 +497,26 @@ __global__ __launch_bounds__(kNT, 1) void step_chunks(const FusedArgs p) {
     // phase 3: every other worker
     for (int w = 0; w < p.W; w++)
       if (w != ch.owner) stream_worker<false>(p, sh, ch, w);
+    {
+      const uint32_t i0 = (tid >> 5) * 256 + (tid & 31) * 8;
+      if (i0 + 8 <= ch.L) {
+        prefetch_l2(p.theta + ch.c0 + i0);
+        prefetch_l2(p.v + ch.c0 + i0);
+      }
+    }
     __syncthreads();
 
     // phase 4: synchronized buffer, second moment, parameters
     update_chunk(p, sh, ch);
+    {
+      const uint64_t cn = c + gridDim.x;
+      if (cn < p.n_ch && !p.chunks) {
+        const uint64_t c0n = cn * p.C;
+        const uint32_t Ln = (uint32_t)((p.N - c0n) < p.C ? (p.N - c0n) : p.C);
+        if ((uint32_t)tid * 2 < (Ln + 31) / 32) prefetch_l2(p.mprev + c0n / 32 + tid * 2);
+        prefetch_worker_tile(p, c0n, Ln, (int)(cn / p.q));
+      }
+    }
     __syncthreads();
   }
 }
