@@ -92,6 +92,8 @@ class OracleRun:
 
 def compare(g: GpuRun, r: OracleRun, what: str = "") -> None:
     """Compare the GPU state with the oracle over the oracle's chunks."""
+    if r.o.n == g.wl.N:
+        return compare_all(g, r, what)
     o, sc, W = r.o, g.sc, g.wl.W
     m_gen = o.mask(0)
     m_used = o.mask(1)
@@ -130,6 +132,29 @@ def compare(g: GpuRun, r: OracleRun, what: str = "") -> None:
                 assert np.array_equal(gi.astype(np.uint64), oidx[start:start + k]), f"idx {tag}"
                 assert_close_exact(f"vals[{w}] {tag}", gv, ov[start:start + k])
         pos += ln
+
+
+def compare_all(g: GpuRun, r: OracleRun, what: str = "") -> None:
+    """compare() when the oracle covers every coordinate: whole arrays at once."""
+    o, sc, W = r.o, g.sc, g.wl.W
+    assert_close_exact(f"theta {what}", sc.read(THETA), o.get(oracle.THETA))
+    assert_close_exact(f"v {what}", sc.read(V), o.get(oracle.V))
+    for w in range(W):
+        assert_close_exact(f"u[{w}] {what}", sc.read(U, w), o.get(oracle.U, w))
+        assert_close_exact(f"e[{w}] {what}", sc.read(E, w), o.get(oracle.E, w))
+    words = sc.mask()
+    ref = oracle.pack_bits(o.mask(0))
+    if not np.array_equal(words, ref):
+        bad = np.nonzero(words != ref)[0]
+        raise AssertionError(f"mask {what}: {bad.size} words differ, first word {bad[0]}")
+    oidx, _ = o.sparse(0)
+    assert oidx.size == sc.K, (what, oidx.size, sc.K)
+    if sc.K:
+        for w in list(range(W)) + [-1]:
+            gi, gv = sc.sparse(w)
+            _, ov = o.sparse(w)
+            assert np.array_equal(gi.astype(np.uint64), oidx), f"idx {what}"
+            assert_close_exact(f"vals[{w}] {what}", gv, ov)
 
 
 def sample_chunks(wl, n_extra: int = 4, seed: int = 0) -> list[int]:

@@ -272,3 +272,33 @@ def test_residuals_in_host_memory():
             compare(g, r, f"step {t}")
     finally:
         g.close()
+
+
+def _random_case(seed):
+    rng = np.random.default_rng(1000 + seed)
+    W = int(rng.integers(1, 10))
+    C = 32 * int(rng.choice([1, 3, 8, 37, 128, 512, 2048]))
+    density = float(rng.choice([0.003, 0.01, 0.05, 0.1, 0.37, 0.5, 1.0]))
+    kind = int(rng.integers(0, 2))
+    per_tensor = bool(rng.integers(0, 2))
+    n_t = int(rng.integers(1, 6))
+    numel = [32 * int(rng.integers(1, 3000)) for _ in range(n_t - 1)] + [int(rng.integers(1, 90000))]
+    wl = synth.Workload(f"rand{seed}", tuple((f"t{i}", (n,)) for i, n in enumerate(numel)), W=W,
+                        chunk=C, densities=(density,), steps=3, kind=kind, sigma=1e-3,
+                        seed=seed)
+    return wl, density, per_tensor
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_shapes(seed):
+    wl, density, per_tensor = _random_case(seed)
+    g = GpuRun(wl, density, flags=CHUNK_PER_TENSOR if per_tensor else 0)
+    r = OracleRun(wl, density, per_tensor=per_tensor)
+    try:
+        for t in range(3):
+            g.step()
+            r.step()
+            compare(g, r, f"seed {seed} step {t}")
+        check_full_mask(g, r)
+    finally:
+        g.close()
