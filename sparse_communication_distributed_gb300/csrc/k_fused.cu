@@ -52,7 +52,12 @@ constexpr uint32_t kCap = 2048;          // candidates ranked in shared memory
 constexpr uint32_t kRankCountMax = 1024; // up to this many: direct rank count
 constexpr int kTB = 47;                  // composite key bits
 
-// dynamic shared memory layout (bytes)
+// Dynamic shared memory layout (bytes), 184.7 KB.  L1 and shared memory share
+// one 256 KB array per SM and loads in flight are staged in L1: this layout
+// sits in the 196 KB carve-out (about 60 KB of L1 left).  Anything past
+// 196 KB moves the kernel to the 228 KB carve-out, where 28 KB of L1 cannot
+// hold enough loads in flight (measured: 24 KB more made the step 16% slower;
+// 24 KB less made no difference).
 constexpr uint32_t kOffKey16 = 0;                      // uint16[65536]
 constexpr uint32_t kOffHist = kOffKey16 + 65536 * 2;   // uint32[4096]
 constexpr uint32_t kOffWprev = kOffHist + 4096 * 4;    // uint32[2048]

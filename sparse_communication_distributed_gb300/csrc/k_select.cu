@@ -52,37 +52,16 @@ struct SelectSmem {
   uint16_t wpre[kMaxWords];
   unsigned long long cand[kCap];
   uint32_t scan[kNT / 32 + 1];
-  uint32_t bin, above, cnt, ncand;
+  uint32_t bin, above, cnt;  // written together by find_bin (3 consecutive words)
+  uint32_t ncand;
 };
 
 enum { SRC_STATE = 0, SRC_BOOT = 1 };
 
-// Sets sm.bin / sm.above / sm.cnt: the bin holding the r-th largest element
-// (1-based) of the histogram, the count in the bins above it, and its count.
-__device__ void find_bin(SelectSmem& sm, int nb, uint32_t r) {
-  const int t = threadIdx.x;
-  const int bpt = nb >= kNT ? nb / kNT : 1;
-  const int b0 = t * bpt;
-  uint32_t s = 0;
-  if (b0 < nb)
-    for (int j = 0; j < bpt; j++) s += sm.hist[b0 + j];
-  uint32_t total;
-  const uint32_t inc = block_incl_scan<kNT>(s, sm.scan, &total);
-  const uint32_t above = total - inc;
-  if (b0 < nb && above < r && r <= above + s) {
-    uint32_t acc = above;
-    for (int j = bpt - 1; j >= 0; j--) {
-      const uint32_t h = sm.hist[b0 + j];
-      if (acc + h >= r) {
-        sm.bin = (uint32_t)(b0 + j);
-        sm.above = acc;
-        sm.cnt = h;
-        break;
-      }
-      acc += h;
-    }
-  }
-  __syncthreads();
+// sm.bin / sm.above / sm.cnt: the bin holding the r-th largest element of
+// the histogram, the count in the bins above it, and its count.
+__device__ __forceinline__ void find_bin(SelectSmem& sm, int nb, uint32_t r) {
+  scape::find_bin<kNT>(sm.hist, nb, r, sm.scan, &sm.bin);
 }
 
 // The four composite keys of quad qd (coordinates 4qd..4qd+3 of the chunk);

@@ -1,6 +1,7 @@
 // Host side of libscape: argument checks, the chunk/shard table, device
 // allocation, the launch sequence of one step and state read-back.  The
 // operations are documented in include/scape.h.
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -15,13 +16,16 @@
 #define SCAPE_API extern "C" __attribute__((visibility("default")))
 
 namespace scape {
+// SM count of the current device (cached per device).
 int num_sms() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
-      n = 148;
+  static std::atomic<int> cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
+  int n = cache[dev].load(std::memory_order_relaxed);
+  if (n <= 0) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      return 152;
+    cache[dev].store(n, std::memory_order_relaxed);
   }
   return n;
 }

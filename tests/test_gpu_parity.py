@@ -110,21 +110,22 @@ def test_loaded_residuals_select_exactly():
         g.close()
 
 
-@pytest.mark.parametrize("n_tied,expect_fallback", [(600, False), (1500, False), (3000, True)])
-def test_tied_bucket_paths(n_tied, expect_fallback):
-    # One 65536 chunk per worker, k = 655: 100 keys of 2.0 and n_tied keys of
-    # 1.0 (the rest 0.5), so the 16-bit bucket of the threshold holds n_tied
-    # tied keys (n_tied > 555 puts the threshold inside it).  600 -> ranked
-    # directly, 1500 -> radix among the candidates, 3000 -> more than the
-    # on-chip list holds, redone by the standalone select.
+@pytest.mark.parametrize("n_high,n_tied,expect_fallback",
+                         [(300, 400, False), (100, 1500, False), (100, 3000, True)])
+def test_tied_bucket_paths(n_high, n_tied, expect_fallback):
+    # One 65536 chunk per worker, k = 655: n_high keys of 2.0 and n_tied keys
+    # of 1.0 (the rest 0.5); n_high < 655 < n_high + n_tied puts the threshold
+    # inside the 16-bit bucket of 1.0, which then holds n_tied tied keys.
+    # 400 -> ranked directly, 1500 -> radix among the on-chip candidates,
+    # 3000 -> more than the on-chip list holds, redone by the standalone select.
     wl = synth.tiny(65536 * 2, 2, 65536, 0.01, beta1=0.0)
     rng = np.random.default_rng(n_tied)
     e0 = np.full((2, wl.N), 0.5, np.float32)
     for w in range(2):
         for c in range(2):
-            pos = c * 65536 + rng.permutation(65536)[: 100 + n_tied]
-            e0[w, pos[:100]] = 2.0
-            e0[w, pos[100:]] = -1.0
+            pos = c * 65536 + rng.permutation(65536)[: n_high + n_tied]
+            e0[w, pos[:n_high]] = 2.0
+            e0[w, pos[n_high:]] = -1.0
     g, r = GpuRun(wl, 0.01), OracleRun(wl, 0.01)
     try:
         for w in range(2):
