@@ -5,6 +5,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <new>
 #include <string>
@@ -56,6 +57,7 @@ struct scape_handle {
   std::vector<ChunkDesc> chunks;     // chunk table (host copy, every mode)
   ChunkDesc* chunks_dev = nullptr;   // device copy, per-tensor mode only
   uint64_t host_bytes = 0;           // page-locked host memory held (residuals)
+  int n_allocs = 0, fail_alloc = -1;  // allocation count, injected failure (tests)
   int prev = 0;               // mask[prev] = M_{t-1} for the next step
   bool has_mask = false;      // a mask exists (built by a step or loaded)
   bool stepped = false;       // compact buffers hold a step's output
@@ -87,9 +89,18 @@ int cuda_fail(scape_handle* h, cudaError_t e, const char* what) {
   return fail(h, SCAPE_ECUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
+// Fault injection for tests: with SCAPE_TEST_FAIL_ALLOC=n in the environment,
+// the n-th device allocation (0-based) of each scape_create reports
+// cudaErrorMemoryAllocation without calling cudaMalloc.
+int fail_alloc_at() {
+  const char* v = std::getenv("SCAPE_TEST_FAIL_ALLOC");
+  return v ? std::atoi(v) : -1;
+}
+
 template <class T>
 cudaError_t dalloc(scape_handle* h, T** p, uint64_t count) {
   const uint64_t bytes = (count ? count : 1) * sizeof(T);
+  if (h->n_allocs++ == h->fail_alloc) return cudaErrorMemoryAllocation;
   cudaError_t e = cudaMalloc(reinterpret_cast<void**>(p), bytes);
   if (e == cudaSuccess) {
     h->device_bytes += bytes;
@@ -224,6 +235,7 @@ SCAPE_API int scape_create_ex(const scape_layout* layout, int W, double density,
 
   scape_handle* h = new (std::nothrow) scape_handle();
   if (!h) return fail(nullptr, SCAPE_ENOMEM, "host allocation failed");
+  h->fail_alloc = fail_alloc_at();
   h->N = N;
   h->C = C;
   h->W = W;

@@ -91,3 +91,13 @@ def test_create_ex_rejects_bad_flags(lib):
     assert lib.scape_create_ex(ctypes.byref(lay), 2, 0.1, 0.9, 0.95, 1e-3, 0.1, 1e-8,
                                scape.CHUNK_PER_TENSOR, ctypes.byref(h)) == scape.SCAPE_EINVAL
     assert "multiple of 32" in lib.scape_last_error(None).decode()
+
+
+def test_injected_allocation_failure_is_reported(lib, monkeypatch):
+    # the first device allocation of scape_create fails: no CUDA call is made,
+    # the handle is not returned and the error says what happened
+    monkeypatch.setenv("SCAPE_TEST_FAIL_ALLOC", "0")
+    rc, h = _create(lib, [4096], 1024, 2, 0.1)
+    assert rc == scape.SCAPE_ENOMEM
+    assert not h.value
+    assert "allocation" in lib.scape_last_error(None).decode()
