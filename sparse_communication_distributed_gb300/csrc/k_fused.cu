@@ -269,31 +269,20 @@ __device__ bool select_chunk(const FusedArgs& p, const Shared& sh, const Chunk& 
     }
   }
 
-  // mask words from the stored keys
-  for (uint32_t j = tid; j < ch.nw; j += kNT) {
-    uint32_t word = 0u;
-    const uint32_t i0 = j * 32;
-    if (i0 + 32 <= L) {
-      const uint4* kp = reinterpret_cast<const uint4*>(sh.key16 + i0);
-#pragma unroll
-      for (int q = 0; q < 4; q++) {
-        const uint4 v = kp[q];
-        const uint32_t h[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int s = 0; s < 4; s++) {
-          const uint32_t lo = h[s] & 0xFFFFu, hi = h[s] >> 16;
-          const uint32_t bit = q * 8 + s * 2;
-          if (lo > T16 || (take_bucket && lo == T16)) word |= 1u << bit;
-          if (hi > T16 || (take_bucket && hi == T16)) word |= 1u << (bit + 1);
-        }
-      }
-    } else {
-      for (uint32_t b = 0; b < 32 && i0 + b < L; b++) {
-        const uint32_t k16 = sh.key16[i0 + b];
-        if (k16 > T16 || (take_bucket && k16 == T16)) word |= 1u << b;
-      }
+  // mask words from the stored keys: each warp builds 32 words by ballot, in
+  // round r its lanes test the 32 coordinates of word j0 + r (consecutive
+  // 16-bit keys, no shared-memory bank conflicts) and lane r keeps the word
+  const int warp = tid >> 5;
+  const uint32_t tb = take_bucket ? T16 : T16 + 1;  // kept iff key16 >= tb
+  for (uint32_t j0 = (uint32_t)warp * 32; j0 < ch.nw; j0 += kNT) {
+    uint32_t mine = 0u;
+    for (int r = 0; r < 32; r++) {
+      const uint32_t i = (j0 + r) * 32 + lane;
+      const bool set = i < L && sh.key16[i] >= tb;
+      const unsigned b = __ballot_sync(kFull, set);
+      if (lane == r) mine = b;
     }
-    sh.mword[j] = word;
+    if (j0 + lane < ch.nw) sh.mword[j0 + lane] = mine;
   }
   __syncthreads();
 
