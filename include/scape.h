@@ -210,6 +210,20 @@ typedef struct {
 
 int scape_mask_stats(scape_handle* h, scape_mask_stats_t* out);
 
+/* ---- Unpack ------------------------------------------------------------------
+ * The receiving side of a compact buffer (the single synchronized sparse
+ * buffer of SCAPE, gist.science technical summary §2; the pages pack masks and
+ * values with dedicated kernels, §2 "Memory Optimization"): scatter
+ *   dense[idx[r]] = vals[r]   for r in [0, K)
+ * into a dense fp32 vector of N coordinates; coordinates not listed are left
+ * as they are (clear dense first for a dense copy of b_w or bbar).  idx, vals
+ * (K entries, e.g. from scape_read_sparse) and dense are DEVICE pointers owned
+ * by the caller; idx entries >= N are skipped and counted into *bad_count (a
+ * DEVICE uint32, may be NULL).  Allocates nothing; enqueues one kernel on
+ * "stream" and returns.  K = 0 is a no-op. */
+int scape_unpack(const uint32_t* idx, const float* vals, uint64_t K, float* dense, uint64_t N,
+                 uint32_t* bad_count, void* stream);
+
 /* ---- Dense AdamS baseline --------------------------------------------------
  * The comparator of the SCAPE pages ("3.26x speedup per step compared to
  * dense AdamS": abstract; gist.science technical summary §4): dense data

@@ -49,3 +49,55 @@ cudaError_t launch_mask_popcount(const uint32_t* a, const uint32_t* b, uint64_t 
 }
 
 }  // namespace scape
+
+// ---- unpack: dense[idx[r]] = vals[r] ----------------------------------------
+
+#include <cstdarg>
+#include <cstdio>
+
+#include "../../include/scape.h"
+
+namespace scape {
+namespace {
+
+__global__ __launch_bounds__(256) void unpack_kernel(const uint32_t* __restrict__ idx,
+                                                     const float* __restrict__ vals, uint64_t K,
+                                                     float* __restrict__ dense, uint64_t N,
+                                                     uint32_t* __restrict__ bad) {
+  const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+  for (uint64_t r = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; r < K; r += stride) {
+    const uint32_t i = idx[r];
+    if (i < N) dense[i] = vals[r];
+    else if (bad) atomicAdd(bad, 1u);  // out-of-range coordinate: skipped and counted
+  }
+}
+
+int unpack_fail(int code, const char* fmt, ...) {
+  char buf[256];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  set_thread_error(buf);
+  return code;
+}
+
+}  // namespace
+}  // namespace scape
+
+extern "C" __attribute__((visibility("default"))) int scape_unpack(
+    const uint32_t* idx, const float* vals, uint64_t K, float* dense, uint64_t N,
+    uint32_t* bad_count, void* stream) {
+  using namespace scape;
+  if (K == 0) return SCAPE_OK;
+  if (!idx || !vals || !dense || N == 0)
+    return unpack_fail(SCAPE_EINVAL, "idx, vals and dense must be device pointers, N > 0");
+  uint64_t grid = (K + 255) / 256;
+  const uint64_t cap = (uint64_t)num_sms() * 8;
+  if (grid > cap) grid = cap;
+  unpack_kernel<<<(unsigned)grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(idx, vals, K, dense,
+                                                                               N, bad_count);
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? SCAPE_OK
+                          : unpack_fail(SCAPE_ECUDA, "unpack: %s", cudaGetErrorString(e));
+}

@@ -24,7 +24,7 @@ CHUNK_PER_TENSOR, RESIDUAL_HOST = 1, 2
 EXPORTS = ("scape_create", "scape_create_ex", "scape_step", "scape_step_host", "scape_mask", "scape_destroy",
            "scape_info", "scape_read_state", "scape_load_state", "scape_read_sparse",
            "scape_last_error", "scape_profile", "scape_profile_read", "scape_step_noalloc",
-           "scape_dense_adams_step", "scape_mask_stats")
+           "scape_dense_adams_step", "scape_mask_stats", "scape_unpack")
 
 
 class ScapeError(RuntimeError):
@@ -93,6 +93,7 @@ def load_library(path: str = LIB_PATH):
                                        ctypes.POINTER(ctypes.c_uint32)]
     lib.scape_step_noalloc.argtypes = [ctypes.POINTER(StepBuffers), ctypes.POINTER(vp), vp]
     lib.scape_mask_stats.argtypes = [vp, ctypes.POINTER(ctypes.c_uint64 * 3)]
+    lib.scape_unpack.argtypes = [vp, vp, u64, vp, u64, vp, vp]
     f32 = ctypes.c_float
     lib.scape_dense_adams_step.argtypes = [vp, vp, vp, ctypes.POINTER(vp), i32, u64, f32, f32, f32,
                                            f32, f32, vp]
@@ -266,5 +267,15 @@ def dense_adams_step(theta, m, v, grads, beta1=0.9, beta2=0.95, lr=1e-3, wd=0.1,
     gp = (ctypes.c_void_p * len(grads))(*[_ptr(g) for g in grads])
     rc = lib.scape_dense_adams_step(_ptr(theta), _ptr(m), _ptr(v), gp, len(grads), theta.numel(),
                                     beta1, beta2, lr, wd, eps, _stream_handle(stream))
+    if rc != SCAPE_OK:
+        raise ScapeError(rc, lib.scape_last_error(None).decode())
+
+
+def unpack(idx, vals, dense, bad_count=None, stream=None) -> None:
+    """scape_unpack on device tensors: dense[idx[r]] = vals[r]."""
+    lib = load_library()
+    rc = lib.scape_unpack(_ptr(idx), _ptr(vals), idx.numel(), _ptr(dense), dense.numel(),
+                          _ptr(bad_count) if bad_count is not None else None,
+                          _stream_handle(stream))
     if rc != SCAPE_OK:
         raise ScapeError(rc, lib.scape_last_error(None).decode())
