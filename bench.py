@@ -179,19 +179,21 @@ def ncu_traffic(kernel: str, N: int):
     return None, None
 
 
-def oracle_sample(wl, density, n_chunks: int, steps: int):
+def oracle_sample(wl, density, n_chunks: int, steps: int, n_batches: int = 2):
     """Time the oracle (as it stands) on n_chunks whole chunks spread over the
-    shards; returns (params/s, seconds, sample params)."""
+    shards, for ``steps`` steps over ``n_batches`` gradient batches used in
+    turn (generated before the timed loop).  Returns (params/s, seconds,
+    sample params, chunks)."""
     import oracle
     nch = -(-wl.N // wl.chunk)
     ids = np.unique(np.linspace(0, nch - 1, n_chunks).astype(np.int64))
     o = oracle.Oracle.for_workload(wl, density, chunk_ids=ids)
     o.set(oracle.THETA, synth.cpu().theta0(wl, o.index))
     grads = [np.stack([synth.cpu().grads(wl, w, t, idx=o.index) for w in range(wl.W)])
-             for t in range(steps)]
+             for t in range(min(n_batches, steps))]
     t0 = time.perf_counter()
     for t in range(steps):
-        o.step(grads[t])
+        o.step(grads[t % len(grads)])
     dt = time.perf_counter() - t0
     return o.n * steps / dt, dt, o.n, ids.size
 
@@ -349,10 +351,12 @@ def run_scape(args, wl, density):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        rate, dt, n, nc = oracle_sample(wl, density, 64 if N > 1 << 24 else 16, 4)
+        n_ch, n_st = (128, 14) if N > 1 << 24 else (16, 8)
+        rate, dt, n, nc = oracle_sample(wl, density, n_ch, n_st)
         cpu = {"value": rate, "unit": "params/s", "cores": 1, "kind": "oracle",
                "sample": f"{nc} whole chunks ({n} params) of {wl.name}, W={W}, density {density}, "
-                         f"4 steps incl. step 0, {dt:.1f} s; single-threaded C++ oracle"}
+                         f"{n_st} steps incl. step 0 over 2 gradient batches, {dt:.1f} s of "
+                         f"oracle time; single-threaded C++ oracle on one host core"}
 
     if rank != 0:
         ranks.close()

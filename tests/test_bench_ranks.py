@@ -54,3 +54,17 @@ def test_reference_arm_prints_on_rank0_only(rank):
         assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["cpu_baseline"]["kind"] == "oracle"
     else:
         assert lines == []
+
+
+def test_algorithmic_bytes_of_the_bench_workload():
+    # per coordinate W*(2 g + 8 u + 8 e + 1/8 mask) + 8 theta + 8 v + 1/8 new mask,
+    # per kept coordinate 8W (vals written and read) + 8 (bbar, idx)
+    sys.path.insert(0, ROOT)
+    import bench
+    import synth
+    wl = synth.WORKLOADS["llama-1.8b-w4"]
+    K = 27090 * 655 + 20  # every full chunk keeps 655, the 2048-long last one 20
+    b = bench.alg_bytes(wl.N, wl.W, K)["step"]
+    assert K == 17_743_970
+    assert abs(b - (wl.N * 88.625 + K * 40)) < 1
+    assert abs(b / 1e9 - 158.052) < 0.001
