@@ -34,6 +34,9 @@
 //     chunk's kept coordinates, read back from the compact buffers the
 //     workers wrote (the only place worker data meets), then v and theta for
 //     every coordinate of the chunk.
+// At step 0 a first launch in boot mode builds M_{-1} the same way: phases 1
+// and 2 on the owner's step-0 accumulator a = e + (b1*u + c1*g), computed
+// read-only, with nothing else written.
 // Arithmetic is the fp32 rule of the library header, with the same
 // parenthesisation and no FMA contraction (built with -fmad=false).
 //
@@ -101,11 +104,18 @@ struct Chunk {
   int owner;
 };
 
+enum { PASS_OTHER = 0, PASS_OWNER = 1, PASS_BOOT = 2 };
+
 // Phases 1 and 3: worker w's streaming pass over the chunk.  One warp per
 // 256-coordinate tile, 8 consecutive coordinates per thread (16-byte loads).
-template <bool OWNER>
+// PASS_OWNER also keeps the keys of |a| and their histogram; PASS_BOOT only
+// computes the step-0 accumulator a = e + (b1*u + c1*g) for its keys and
+// writes nothing to memory.
+template <int PASS>
 __device__ __forceinline__ void stream_worker(const FusedArgs& p, const Shared& sh,
                                               const Chunk& ch, int w) {
+  constexpr bool KEYS = PASS != PASS_OTHER;
+  constexpr bool WRITE = PASS != PASS_BOOT;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const uint16_t* __restrict__ g = p.grads[w] + ch.c0;
   float* __restrict__ u = p.u + (uint64_t)w * p.Np + ch.c0;
@@ -116,11 +126,14 @@ __device__ __forceinline__ void stream_worker(const FusedArgs& p, const Shared& 
   for (uint32_t t = warp; t < ntile; t += kNW) {
     const uint32_t i0 = t * 256 + lane * 8;
     if (i0 >= ch.L) continue;
-    const uint32_t j = i0 >> 5;
-    const uint32_t word = sh.wprev[j];
-    const uint32_t sft = (lane & 3) * 8;
-    const uint32_t byte = (word >> sft) & 0xFFu;
-    const uint32_t rank0 = sh.wpre[j] + __popc(word & ((1u << sft) - 1u));
+    uint32_t byte = 0, rank0 = 0;
+    if (WRITE) {
+      const uint32_t j = i0 >> 5;
+      const uint32_t word = sh.wprev[j];
+      const uint32_t sft = (lane & 3) * 8;
+      byte = (word >> sft) & 0xFFu;
+      rank0 = sh.wpre[j] + __popc(word & ((1u << sft) - 1u));
+    }
     if (i0 + 8 <= ch.L) {
       const uint4 gr = ld_stream_u4(g + i0);
       float4* up = reinterpret_cast<float4*>(u + i0);
@@ -135,22 +148,26 @@ __device__ __forceinline__ void stream_worker(const FusedArgs& p, const Shared& 
       for (int jj = 0; jj < 8; jj++) {
         const float un = (b1 * uu[jj]) + (c1 * gf[jj]);
         const float a = ee[jj] + un;
-        const bool m = (byte >> jj) & 1u;
-        const float b = m ? a : 0.0f;
-        uu[jj] = un;
-        ee[jj] = a - b;
-        if (m) vals[rank0 + __popc(byte & ((1u << jj) - 1u))] = b;
-        if (OWNER) {
+        if (WRITE) {
+          const bool m = (byte >> jj) & 1u;
+          const float b = m ? a : 0.0f;
+          uu[jj] = un;
+          ee[jj] = a - b;
+          if (m) vals[rank0 + __popc(byte & ((1u << jj) - 1u))] = b;
+        }
+        if (KEYS) {
           const uint32_t key = __float_as_uint(a) & 0x7FFFFFFFu;
           k16[jj] = key >> 15;
           atomicAdd(&sh.hist[key >> 19], 1u);
         }
       }
-      up[0] = make_float4(uu[0], uu[1], uu[2], uu[3]);
-      up[1] = make_float4(uu[4], uu[5], uu[6], uu[7]);
-      ep[0] = make_float4(ee[0], ee[1], ee[2], ee[3]);
-      ep[1] = make_float4(ee[4], ee[5], ee[6], ee[7]);
-      if (OWNER) {
+      if (WRITE) {
+        up[0] = make_float4(uu[0], uu[1], uu[2], uu[3]);
+        up[1] = make_float4(uu[4], uu[5], uu[6], uu[7]);
+        ep[0] = make_float4(ee[0], ee[1], ee[2], ee[3]);
+        ep[1] = make_float4(ee[4], ee[5], ee[6], ee[7]);
+      }
+      if (KEYS) {
         uint4 kv;
         kv.x = k16[0] | (k16[1] << 16);
         kv.y = k16[2] | (k16[3] << 16);
@@ -163,12 +180,14 @@ __device__ __forceinline__ void stream_worker(const FusedArgs& p, const Shared& 
       for (uint32_t jj = 0; jj < nv; jj++) {
         const float un = (b1 * u[i0 + jj]) + (c1 * bf16f(g[i0 + jj]));
         const float a = e[i0 + jj] + un;
-        const bool m = (byte >> jj) & 1u;
-        const float b = m ? a : 0.0f;
-        u[i0 + jj] = un;
-        e[i0 + jj] = a - b;
-        if (m) vals[rank0 + __popc(byte & ((1u << jj) - 1u))] = b;
-        if (OWNER) {
+        if (WRITE) {
+          const bool m = (byte >> jj) & 1u;
+          const float b = m ? a : 0.0f;
+          u[i0 + jj] = un;
+          e[i0 + jj] = a - b;
+          if (m) vals[rank0 + __popc(byte & ((1u << jj) - 1u))] = b;
+        }
+        if (KEYS) {
           const uint32_t key = __float_as_uint(a) & 0x7FFFFFFFu;
           sh.key16[i0 + jj] = (uint16_t)(key >> 15);
           atomicAdd(&sh.hist[key >> 19], 1u);
@@ -179,9 +198,15 @@ __device__ __forceinline__ void stream_worker(const FusedArgs& p, const Shared& 
 }
 
 // Full 31-bit key of the owner's accumulator at chunk coordinate i, rebuilt
-// from what phase 1 wrote: the kept value on M_{t-1}, else the residual.
+// from what phase 1 wrote: the kept value on M_{t-1}, else the residual (or,
+// in the step-0 pass, recomputed from the untouched state and gradient).
 __device__ __forceinline__ uint32_t owner_key(const FusedArgs& p, const Shared& sh,
                                               const Chunk& ch, uint32_t i) {
+  if (p.boot) {  // step 0: nothing written yet, a = e + (b1*u + c1*g)
+    const uint64_t x = (uint64_t)ch.owner * p.Np + ch.c0 + i;
+    const float un = (p.b1 * p.u[x]) + (p.c1 * bf16f(p.grads[ch.owner][ch.c0 + i]));
+    return __float_as_uint(p.e[x] + un) & 0x7FFFFFFFu;
+  }
   const uint32_t j = i >> 5, bit = i & 31;
   const uint32_t word = sh.wprev[j];
   float a;
@@ -456,10 +481,13 @@ __global__ __launch_bounds__(kNT, 1) void step_chunks(const FusedArgs p) {
 
     // phase 0: M_{t-1} words of the chunk, their popcount prefix; clear the histogram
     {
-      const uint32_t* mp = p.mprev + ch.c0 / 32;
       const uint32_t j0 = tid * 2;
-      const uint32_t w0 = j0 < ch.nw ? mp[j0] : 0u;
-      const uint32_t w1 = j0 + 1 < ch.nw ? mp[j0 + 1] : 0u;
+      uint32_t w0 = 0u, w1 = 0u;
+      if (!p.boot) {  // no M_{t-1} at step 0
+        const uint32_t* mp = p.mprev + ch.c0 / 32;
+        if (j0 < ch.nw) w0 = mp[j0];
+        if (j0 + 1 < ch.nw) w1 = mp[j0 + 1];
+      }
       const uint32_t cnt = __popc(w0) + __popc(w1);
       uint32_t total;
       const uint32_t inc = block_incl_scan<kNT>(cnt, sh.scan, &total);
@@ -473,8 +501,25 @@ __global__ __launch_bounds__(kNT, 1) void step_chunks(const FusedArgs p) {
       __syncthreads();
     }
 
+    if (p.boot) {
+      // step 0, first launch: M_{-1} of this chunk from the owner's step-0
+      // accumulator (read only), ranked on chip like M_t below
+      stream_worker<PASS_BOOT>(p, sh, ch, ch.owner);
+      __syncthreads();
+      const bool ok = select_chunk(p, sh, ch);
+      if (ok) {
+        uint32_t* mo = p.mout + ch.c0 / 32;
+        for (uint32_t j = tid; j < ch.nw; j += kNT) mo[j] = sh.mword[j];
+      } else if (tid == 0) {
+        p.fallback[c] = 1u;
+        atomicAdd(p.n_fallback, 1u);
+      }
+      __syncthreads();
+      continue;
+    }
+
     // phase 1: the owner's pass, keeping its keys
-    stream_worker<true>(p, sh, ch, ch.owner);
+    stream_worker<PASS_OWNER>(p, sh, ch, ch.owner);
     if (p.W > 1) prefetch_worker_tile(p, ch.c0, ch.L, ch.owner == 0 ? 1 : 0);
     __syncthreads();
 
@@ -490,7 +535,7 @@ __global__ __launch_bounds__(kNT, 1) void step_chunks(const FusedArgs p) {
 
     // phase 3: every other worker
     for (int w = 0; w < p.W; w++)
-      if (w != ch.owner) stream_worker<false>(p, sh, ch, w);
+      if (w != ch.owner) stream_worker<PASS_OTHER>(p, sh, ch, w);
     {
       const uint32_t i0 = (tid >> 5) * 256 + (tid & 31) * 8;
       if (i0 + 8 <= ch.L) {
@@ -504,7 +549,7 @@ __global__ __launch_bounds__(kNT, 1) void step_chunks(const FusedArgs p) {
     update_chunk(p, sh, ch);
     {
       const uint64_t cn = c + gridDim.x;
-      if (cn < p.n_ch && !p.chunks) {
+      if (cn < p.n_ch && !p.chunks && !p.boot) {
         const uint64_t c0n = cn * p.C;
         const uint32_t Ln = (uint32_t)((p.N - c0n) < p.C ? (p.N - c0n) : p.C);
         if ((uint32_t)tid * 2 < (Ln + 31) / 32) prefetch_l2(p.mprev + c0n / 32 + tid * 2);

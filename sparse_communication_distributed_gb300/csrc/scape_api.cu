@@ -368,6 +368,43 @@ SCAPE_API int scape_info(const scape_handle* h, scape_info_t* out) {
   return SCAPE_OK;
 }
 
+// Arguments of the fused step kernel (normal mode).
+static void fill_fused(const scape_handle* h, const uint16_t* const* g, const uint32_t* mprev,
+                       uint32_t* mout, FusedArgs& a) {
+  a = FusedArgs{};
+  for (int w = 0; w < h->W; w++) a.grads[w] = g[w];
+  a.u = h->u;
+  a.e = h->e;
+  a.vals = h->vals;
+  a.theta = h->theta;
+  a.v = h->v;
+  a.bbar = h->bbar;
+  a.idx = h->idx;
+  a.mprev = mprev;
+  a.mout = mout;
+  a.fallback = h->fallback;
+  a.n_fallback = h->n_fallback;
+  a.chunks = h->chunks_dev;
+  a.N = h->N;
+  a.Np = h->Np;
+  a.Kp = h->Kp;
+  a.n_ch = h->n_ch;
+  a.q = h->q;
+  a.C = h->C;
+  a.k_full = h->k_full;
+  a.k_last = h->k_last;
+  a.W = h->W;
+  a.boot = 0;
+  a.b1 = h->b1;
+  a.c1 = h->c1;
+  a.b2 = h->b2;
+  a.c2 = h->c2;
+  a.lr = h->lr;
+  a.wd = h->wd;
+  a.eps = h->eps;
+  a.invW = h->invW;
+}
+
 static int step_device(scape_handle* h, const uint16_t* const* g, cudaStream_t s) {
   cudaError_t e;
   uint32_t* mprev = h->mask[h->prev];
@@ -390,46 +427,21 @@ static int step_device(scape_handle* h, const uint16_t* const* g, cudaStream_t s
   sa.k_last = h->k_last;
   sa.chunks = h->chunks_dev;
 
+  FusedArgs a{};
   if (!h->has_mask) {  // step 0: M_{-1} from the step-0 accumulators
     PhaseTimer pt(h, SCAPE_PH_SELECT_BOOT, s);
-    sa.mprev = nullptr;
+    fill_fused(h, g, mprev, mprev, a);
+    a.mprev = nullptr;
+    a.boot = 1;
+    if ((e = launch_step_chunks(a, s)) != cudaSuccess) return cuda_fail(h, e, "step-0 mask");
+    sa.mprev = nullptr;  // chunks with too many tied keys: the standalone select
     sa.mout = mprev;
-    sa.flags = nullptr;
+    sa.flags = h->fallback;
     if ((e = launch_select(sa, true, s)) != cudaSuccess) return cuda_fail(h, e, "select (step 0)");
     pt.done();
   }
   {
-    FusedArgs a{};
-    for (int w = 0; w < h->W; w++) a.grads[w] = g[w];
-    a.u = h->u;
-    a.e = h->e;
-    a.vals = h->vals;
-    a.theta = h->theta;
-    a.v = h->v;
-    a.bbar = h->bbar;
-    a.idx = h->idx;
-    a.mprev = mprev;
-    a.mout = mcur;
-    a.fallback = h->fallback;
-    a.n_fallback = h->n_fallback;
-    a.chunks = h->chunks_dev;
-    a.N = h->N;
-    a.Np = h->Np;
-    a.Kp = h->Kp;
-    a.n_ch = h->n_ch;
-    a.q = h->q;
-    a.C = h->C;
-    a.k_full = h->k_full;
-    a.k_last = h->k_last;
-    a.W = h->W;
-    a.b1 = h->b1;
-    a.c1 = h->c1;
-    a.b2 = h->b2;
-    a.c2 = h->c2;
-    a.lr = h->lr;
-    a.wd = h->wd;
-    a.eps = h->eps;
-    a.invW = h->invW;
+    fill_fused(h, g, mprev, mcur, a);
     PhaseTimer pt(h, SCAPE_PH_STEP, s);
     if ((e = launch_step_chunks(a, s)) != cudaSuccess) return cuda_fail(h, e, "step kernel");
     pt.done();

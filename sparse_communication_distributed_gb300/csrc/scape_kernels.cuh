@@ -45,6 +45,7 @@ struct FusedArgs {
   uint64_t N, Np, Kp, n_ch, q;
   uint32_t C, k_full, k_last;
   int W;
+  int boot;  // 1: only build M_{-1} into mout from the step-0 accumulators (no writes)
   float b1, c1, b2, c2, lr, wd, eps, invW;
 };
 
