@@ -53,7 +53,8 @@ typedef struct scape_handle scape_handle; /* opaque, owned by the library */
 
 /* Flat parameter layout: the concatenation of n_tensors tensors of numel[]
  * coordinates (N = sum numel).  Chunks tile the flat vector and ignore tensor
- * boundaries. numel is read during scape_create only. */
+ * boundaries, unless scape_create_ex is given SCAPE_CHUNK_PER_TENSOR.  numel
+ * is read during scape_create only. */
 typedef struct {
   uint32_t n_tensors;
   const uint64_t* numel;
@@ -101,7 +102,7 @@ typedef struct {
   uint64_t N;          /* coordinates */
   uint32_t W;          /* emulated workers */
   uint32_t chunk;      /* C */
-  uint64_t n_chunks;   /* ceil(N / C) */
+  uint64_t n_chunks;   /* ceil(N / C); with SCAPE_CHUNK_PER_TENSOR the sum over tensors */
   uint64_t chunks_per_worker; /* q */
   uint32_t k_full;     /* k of a full chunk */
   uint32_t k_last;     /* k of the last chunk */
@@ -118,7 +119,9 @@ typedef struct {
 /* Create a handle: computes the chunk/shard table, allocates all state on the
  * current CUDA device (theta, v: N fp32; u, e: W x N fp32; two N-bit masks;
  * K-entry compact buffers) and zeroes it.  Set theta with scape_load_state.
- * On failure *out is NULL and nothing is leaked. */
+ * On failure *out is NULL and nothing is leaked.  For tests of that path,
+ * SCAPE_TEST_FAIL_ALLOC=n in the environment makes the n-th (0-based) device
+ * allocation of each create fail with SCAPE_ENOMEM. */
 int scape_create(const scape_layout* layout, int W, double density, float beta1, float beta2,
                  float lr, float wd, float eps, scape_handle** out);
 
@@ -175,8 +178,9 @@ int scape_read_sparse(scape_handle* h, int w, uint32_t* idx, float* vals, uint64
                       uint64_t count, uint64_t* total);
 
 /* Message of the handle's last error ("" if none).  Valid until the next call
- * on the handle.  h == NULL gives the message of the last failed
- * scape_create on this thread. */
+ * on the handle.  h == NULL gives the message of the last failure, on this
+ * thread, of a call that has no handle: scape_create, scape_create_ex,
+ * scape_unpack, scape_dense_adams_step, scape_step_noalloc. */
 const char* scape_last_error(const scape_handle* h);
 
 /* enable != 0: every later step records CUDA events around each kernel phase
