@@ -395,6 +395,11 @@ __device__ __forceinline__ void prefetch_worker_tile(const FusedArgs& p, uint64_
 }
 
 // Phase 4: fixed-order W-way sum of the compact buffers and the AdamS update.
+// The kept coordinates of a 256-coordinate tile have consecutive packed
+// positions [R0, R0 + cnt), so the warp computes their bbar together: lane l
+// takes positions R0 + l, R0 + l + 32, ... (coalesced reads of the W rows, one
+// memory round trip per 32 kept coordinates) and hands each value to the lane
+// that holds the coordinate with a shuffle.
 __device__ __forceinline__ void update_chunk(const FusedArgs& p, const Shared& sh,
                                              const Chunk& ch) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -402,15 +407,40 @@ __device__ __forceinline__ void update_chunk(const FusedArgs& p, const Shared& s
   float* __restrict__ vv = p.v + ch.c0;
   const float b2 = p.b2, c2 = p.c2, lr = p.lr, wd = p.wd, eps = p.eps, invW = p.invW;
   const uint32_t ntile = (ch.L + 255) / 256;
-  for (uint32_t t = warp; t < ntile; t += kNW) {
+  for (uint32_t t = warp; t < ntile; t += kNW) {  // warp-uniform: every lane takes part
     const uint32_t i0 = t * 256 + lane * 8;
-    if (i0 >= ch.L) continue;
-    const uint32_t j = i0 >> 5;
-    const uint32_t word = sh.wprev[j];
-    const uint32_t sft = (lane & 3) * 8;
-    const uint32_t byte = (word >> sft) & 0xFFu;
-    const uint32_t rank0 = (uint32_t)ch.base + sh.wpre[j] + __popc(word & ((1u << sft) - 1u));
-    const uint32_t nv = (ch.L - i0) < 8 ? (ch.L - i0) : 8;
+    const bool active = i0 < ch.L;
+    uint32_t byte = 0, local0 = 0;
+    if (active) {
+      const uint32_t j = i0 >> 5;
+      const uint32_t word = sh.wprev[j];
+      const uint32_t sft = (lane & 3) * 8;
+      byte = (word >> sft) & 0xFFu;
+      local0 = sh.wpre[j] + __popc(word & ((1u << sft) - 1u));
+    }
+    const uint32_t tile0 = sh.wpre[t * 8];  // in-chunk position of the tile's first kept value
+    const uint32_t cnt = __reduce_add_sync(kFull, (uint32_t)__popc(byte));
+    const uint32_t nv = active ? ((ch.L - i0) < 8 ? (ch.L - i0) : 8) : 0;
+    if (nv == 8) {  // theta and v travel to L2 while bbar is being summed
+      prefetch_l2(th + i0);
+      prefetch_l2(vv + i0);
+    }
+    // bbar of the tile's kept coordinates, computed cooperatively
+    float bb[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    const uint32_t R0 = (uint32_t)ch.base + tile0;
+    for (uint32_t r0 = 0; r0 < cnt; r0 += 32) {
+      float mine = 0.0f;
+      if (r0 + lane < cnt) {
+        mine = ordered_sum(p, R0 + r0 + lane) * invW;
+        p.bbar[R0 + r0 + lane] = mine;
+      }
+#pragma unroll
+      for (int jj = 0; jj < 8; jj++) {
+        const uint32_t need = local0 - tile0 + __popc(byte & ((1u << jj) - 1u));
+        const float got = __shfl_sync(kFull, mine, need & 31);
+        if (((byte >> jj) & 1u) && need >= r0 && need < r0 + 32) bb[jj] = got;
+      }
+    }
     float tt[8], vo[8];
     if (nv == 8) {
       const float4 t0 = reinterpret_cast<const float4*>(th + i0)[0];
@@ -422,6 +452,7 @@ __device__ __forceinline__ void update_chunk(const FusedArgs& p, const Shared& s
       vo[0] = v0.x; vo[1] = v0.y; vo[2] = v0.z; vo[3] = v0.w;
       vo[4] = v1.x; vo[5] = v1.y; vo[6] = v1.z; vo[7] = v1.w;
     } else {
+#pragma unroll
       for (uint32_t jj = 0; jj < 8; jj++) {
         tt[jj] = jj < nv ? th[i0 + jj] : 0.0f;
         vo[jj] = jj < nv ? vv[i0 + jj] : 0.0f;
@@ -430,15 +461,10 @@ __device__ __forceinline__ void update_chunk(const FusedArgs& p, const Shared& s
 #pragma unroll
     for (int jj = 0; jj < 8; jj++) {
       const bool m = (byte >> jj) & 1u;
-      float bb = 0.0f;
-      if (m) {
-        const uint32_t r = rank0 + __popc(byte & ((1u << jj) - 1u));
-        bb = ordered_sum(p, r) * invW;
-        p.bbar[r] = bb;
-        p.idx[r] = (uint32_t)(ch.c0 + i0 + jj);
-      }
-      const float vn = (b2 * vo[jj]) + (c2 * (bb * bb));
-      const float q = m ? bb / (sqrtf(vn) + eps) : 0.0f;
+      if (m) p.idx[R0 + local0 - tile0 + __popc(byte & ((1u << jj) - 1u))] =
+          (uint32_t)(ch.c0 + i0 + jj);
+      const float vn = (b2 * vo[jj]) + (c2 * (bb[jj] * bb[jj]));
+      const float q = m ? bb[jj] / (sqrtf(vn) + eps) : 0.0f;
       vo[jj] = vn;
       tt[jj] = tt[jj] - (lr * (q + (wd * tt[jj])));
     }
@@ -448,10 +474,12 @@ __device__ __forceinline__ void update_chunk(const FusedArgs& p, const Shared& s
       reinterpret_cast<float4*>(vv + i0)[0] = make_float4(vo[0], vo[1], vo[2], vo[3]);
       reinterpret_cast<float4*>(vv + i0)[1] = make_float4(vo[4], vo[5], vo[6], vo[7]);
     } else {
-      for (uint32_t jj = 0; jj < nv; jj++) {
-        th[i0 + jj] = tt[jj];
-        vv[i0 + jj] = vo[jj];
-      }
+#pragma unroll
+      for (uint32_t jj = 0; jj < 8; jj++)
+        if (jj < nv) {
+          th[i0 + jj] = tt[jj];
+          vv[i0 + jj] = vo[jj];
+        }
     }
   }
 }
