@@ -55,7 +55,7 @@ constexpr uint32_t kCap = 2048;          // candidates ranked in shared memory
 constexpr uint32_t kRankCountMax = 1024; // up to this many: direct rank count
 constexpr int kTB = 47;                  // composite key bits
 
-// Dynamic shared memory layout (bytes), 184.7 KB.  L1 and shared memory share
+// Dynamic shared memory layout (bytes), 188.8 KB.  L1 and shared memory share
 // one 256 KB array per SM and loads in flight are staged in L1: this layout
 // sits in the 196 KB carve-out (about 60 KB of L1 left).  Anything past
 // 196 KB moves the kernel to the 228 KB carve-out, where 28 KB of L1 cannot
@@ -69,7 +69,8 @@ constexpr uint32_t kOffWpre = kOffMword + 2048 * 4;    // uint16[2048]
 constexpr uint32_t kOffCand = kOffWpre + 2048 * 2;     // uint64[kCap]
 constexpr uint32_t kOffScan = kOffCand + kCap * 8;     // uint32[64]
 constexpr uint32_t kOffCtl = kOffScan + 64 * 4;        // uint32[32]
-constexpr uint32_t kSmemBytes = kOffCtl + 32 * 4;
+constexpr uint32_t kOffStage = kOffCtl + 32 * 4;       // float[32 warps][32]
+constexpr uint32_t kSmemBytes = kOffStage + kNW * 32 * 4;
 
 // ctl[] slots
 enum { C_BIN = 0, C_ABOVE = 1, C_CNT = 2, C_NCAND = 3, C_SUB = 8 /* 16 entries */ };
@@ -83,6 +84,7 @@ struct Shared {
   unsigned long long* cand;
   uint32_t* scan;
   uint32_t* ctl;
+  float* stage;  // per warp: the tile's first 32 kept values, for one coalesced store
 };
 
 __device__ __forceinline__ Shared carve(unsigned char* s) {
@@ -95,6 +97,7 @@ __device__ __forceinline__ Shared carve(unsigned char* s) {
   sh.cand = reinterpret_cast<unsigned long long*>(s + kOffCand);
   sh.scan = reinterpret_cast<uint32_t*>(s + kOffScan);
   sh.ctl = reinterpret_cast<uint32_t*>(s + kOffCtl);
+  sh.stage = reinterpret_cast<float*>(s + kOffStage);
   return sh;
 }
 
@@ -122,19 +125,32 @@ __device__ __forceinline__ void stream_worker(const FusedArgs& p, const Shared& 
   float* __restrict__ e = p.e + (uint64_t)w * p.Np + ch.c0;
   float* __restrict__ vals = p.vals + (uint64_t)w * p.Kp + ch.base;
   const float b1 = p.b1, c1 = p.c1;
+  float* stage = sh.stage + warp * 32;
   const uint32_t ntile = (ch.L + 255) / 256;
-  for (uint32_t t = warp; t < ntile; t += kNW) {
+  for (uint32_t t = warp; t < ntile; t += kNW) {  // warp-uniform: every lane takes part
     const uint32_t i0 = t * 256 + lane * 8;
-    if (i0 >= ch.L) continue;
-    uint32_t byte = 0, rank0 = 0;
+    const bool active = i0 < ch.L;
+    uint32_t byte = 0, rank0 = 0, tile0 = 0;
     if (WRITE) {
-      const uint32_t j = i0 >> 5;
-      const uint32_t word = sh.wprev[j];
-      const uint32_t sft = (lane & 3) * 8;
-      byte = (word >> sft) & 0xFFu;
-      rank0 = sh.wpre[j] + __popc(word & ((1u << sft) - 1u));
+      if (active) {
+        const uint32_t j = i0 >> 5;
+        const uint32_t word = sh.wprev[j];
+        const uint32_t sft = (lane & 3) * 8;
+        byte = (word >> sft) & 0xFFu;
+        rank0 = sh.wpre[j] + __popc(word & ((1u << sft) - 1u));
+      }
+      tile0 = sh.wpre[t * 8];  // the tile's kept values occupy [tile0, tile0 + cnt)
     }
-    if (i0 + 8 <= ch.L) {
+    // kept value of element jj: tile rank < 32 -> staged, else stored directly
+#define SCAPE_KEEP(jj, bval)                                              \
+    do {                                                                  \
+      const uint32_t r_ = rank0 + __popc(byte & ((1u << (jj)) - 1u));     \
+      if (r_ - tile0 < 32u) stage[r_ - tile0] = (bval);                   \
+      else vals[r_] = (bval);                                             \
+    } while (0)
+    if (!active) {
+      // nothing to stream; the lane still joins the warp's coalesced store
+    } else if (i0 + 8 <= ch.L) {
       const uint4 gr = ld_stream_u4(g + i0);
       float4* up = reinterpret_cast<float4*>(u + i0);
       float4* ep = reinterpret_cast<float4*>(e + i0);
@@ -153,7 +169,7 @@ __device__ __forceinline__ void stream_worker(const FusedArgs& p, const Shared& 
           const float b = m ? a : 0.0f;
           uu[jj] = un;
           ee[jj] = a - b;
-          if (m) vals[rank0 + __popc(byte & ((1u << jj) - 1u))] = b;
+          if (m) SCAPE_KEEP(jj, b);
         }
         if (KEYS) {
           const uint32_t key = __float_as_uint(a) & 0x7FFFFFFFu;
@@ -185,7 +201,7 @@ __device__ __forceinline__ void stream_worker(const FusedArgs& p, const Shared& 
           const float b = m ? a : 0.0f;
           u[i0 + jj] = un;
           e[i0 + jj] = a - b;
-          if (m) vals[rank0 + __popc(byte & ((1u << jj) - 1u))] = b;
+          if (m) SCAPE_KEEP(jj, b);
         }
         if (KEYS) {
           const uint32_t key = __float_as_uint(a) & 0x7FFFFFFFu;
@@ -193,6 +209,13 @@ __device__ __forceinline__ void stream_worker(const FusedArgs& p, const Shared& 
           atomicAdd(&sh.hist[key >> 19], 1u);
         }
       }
+    }
+#undef SCAPE_KEEP
+    if (WRITE) {
+      const uint32_t cnt = __reduce_add_sync(kFull, (uint32_t)__popc(byte));
+      __syncwarp();
+      if (lane < cnt) vals[tile0 + lane] = stage[lane];
+      __syncwarp();
     }
   }
 }
