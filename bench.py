@@ -39,7 +39,7 @@ def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--warmup", type=int, default=3, help=">= 1; the first warm-up step is step 0")
     ap.add_argument("--impl", default="scape", choices=["scape", "reference"])
     ap.add_argument("--workload", default=synth.BENCH_WORKLOAD, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--density", type=float, default=None)
@@ -252,7 +252,14 @@ def run_scape(args, wl, density):
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream(dev)
 
-    for i in range(args.warmup):
+    # step 0 (the step-0 mask plus the first step), timed on its own
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    sc.step(batches[0], stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    step0_ms = e0.elapsed_time(e1)
+    for i in range(1, args.warmup):
         sc.step(batches[i % n_batches], stream)
     torch.cuda.synchronize()
 
@@ -398,6 +405,7 @@ def run_scape(args, wl, density):
                      "peak_kind": f"{peak_kind} (hbm_gbs)"},
         "kernels_ms_per_step": {k: v[0] / args.steps for k, v in phases.items() if v[1]},
         "gpu_launches": args.steps * 2,
+        "step0_ms": step0_ms,
         "select_fallback_chunks": sc._info()["select_fallbacks"],
         "clocks": clk,
         "e2e": e2e,
@@ -411,6 +419,8 @@ def run_scape(args, wl, density):
 
 def main():
     args = parse()
+    if args.impl == "scape" and args.warmup < 1:
+        raise SystemExit("--warmup must be >= 1 (the first warm-up step is step 0)")
     wl = synth.WORKLOADS[args.workload]
     if args.workers is not None:
         import dataclasses
