@@ -114,6 +114,14 @@ typedef struct {
                                 redid because their threshold bucket held too many ties */
   uint32_t flags;      /* scape_create_ex options */
   uint64_t host_bytes; /* page-locked host memory held (SCAPE_RESIDUAL_HOST) */
+  /* Debug builds (libscape_debug.so, compiled with SCAPE_DEBUG_CHECKS) check in
+   * the kernels every index that depends on the applied mask carrying exactly
+   * k_c bits per chunk; a failed check skips the access and is recorded here.
+   * Release builds report checks_compiled = 0 and zeros. */
+  uint32_t checks_compiled;
+  uint32_t check_code;  /* first failed check (0 = none) */
+  uint32_t check_count; /* failed checks so far */
+  uint64_t check_where; /* coordinate of the first failure */
 } scape_info_t;
 
 /* Create a handle: computes the chunk/shard table, allocates all state on the
@@ -165,7 +173,9 @@ int scape_read_state(scape_handle* h, int which, int w, void* dst, uint64_t offs
 /* Overwrite elements [offset, offset+count) of a state field from src (host
  * or device).  A MASK load must cover all words and carry exactly k_c bits in
  * every chunk (checked; SCAPE_EINVAL otherwise); it becomes the mask the next
- * step applies, so that step does no step-0 selection.  STEP sets t. */
+ * step applies, so that step does no step-0 selection.  STEP sets t.
+ * (SCAPE_TEST_SKIP_MASK_CHECK=1 in the environment skips the mask check; it
+ * exists for tests of the debug build's kernel checks.) */
 int scape_load_state(scape_handle* h, int which, int w, const void* src, uint64_t offset,
                      uint64_t count);
 

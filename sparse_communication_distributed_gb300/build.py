@@ -12,6 +12,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libscape.so")
+DEBUG_LIB = os.path.join(HERE, "libscape_debug.so")
 SOURCES = ["scape_api.cu", "k_fused.cu", "k_select.cu", "k_dense.cu", "k_maskops.cu",
            "scape_noalloc.cu"]
 
@@ -29,13 +30,20 @@ def nvcc() -> str:
     return cand if os.path.exists(cand) else "nvcc"
 
 
-def build(ptxas_verbose: bool = False, out: str = LIB) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build(ptxas_verbose: bool = False, out: str = LIB, debug_checks: bool = False) -> str:
+    """Compile libscape.so; debug_checks builds libscape_debug.so, whose
+    kernels check mask-dependent indexes (SCAPE_DEBUG_CHECKS)."""
+    if debug_checks and out == LIB:
+        out = DEBUG_LIB
+    bdir = os.path.join(BUILD, "debug" if debug_checks else "release")
+    os.makedirs(bdir, exist_ok=True)
     extra = ["-Xptxas", "-v"] if ptxas_verbose else []
+    if debug_checks:
+        extra += ["-DSCAPE_DEBUG_CHECKS"]
     procs = []
     objs = []
     for src in SOURCES:
-        obj = os.path.join(BUILD, src.replace(".cu", ".o"))
+        obj = os.path.join(bdir, src.replace(".cu", ".o"))
         objs.append(obj)
         cmd = [nvcc()] + NVCC_FLAGS + extra + ["-c", os.path.join(CSRC, src), "-o", obj]
         procs.append((cmd, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)))
@@ -55,5 +63,5 @@ def build(ptxas_verbose: bool = False, out: str = LIB) -> str:
 
 
 if __name__ == "__main__":
-    build(ptxas_verbose="--ptxas-verbose" in sys.argv)
-    print(LIB)
+    print(build(ptxas_verbose="--ptxas-verbose" in sys.argv,
+                debug_checks="--debug-checks" in sys.argv))

@@ -146,7 +146,8 @@ __device__ __forceinline__ void stream_worker(const FusedArgs& p, const Shared& 
     do {                                                                  \
       const uint32_t r_ = rank0 + __popc(byte & ((1u << (jj)) - 1u));     \
       if (r_ - tile0 < 32u) stage[r_ - tile0] = (bval);                   \
-      else vals[r_] = (bval);                                             \
+      else if (SCAPE_CHECK(p.dbg, r_ < ch.k, CHK_VALS_WRITE,              \
+                           ch.c0 + i0 + (jj))) vals[r_] = (bval);         \
     } while (0)
     if (!active) {
       // nothing to stream; the lane still joins the warp's coalesced store
@@ -214,7 +215,8 @@ __device__ __forceinline__ void stream_worker(const FusedArgs& p, const Shared& 
     if (WRITE) {
       const uint32_t cnt = __reduce_add_sync(kFull, (uint32_t)__popc(byte));
       __syncwarp();
-      if (lane < cnt) vals[tile0 + lane] = stage[lane];
+      if (lane < cnt && SCAPE_CHECK(p.dbg, tile0 + lane < ch.k, CHK_VALS_STAGE, ch.c0 + t * 256))
+        vals[tile0 + lane] = stage[lane];
       __syncwarp();
     }
   }
@@ -235,7 +237,9 @@ __device__ __forceinline__ uint32_t owner_key(const FusedArgs& p, const Shared& 
   float a;
   if ((word >> bit) & 1u) {
     const uint32_t r = sh.wpre[j] + __popc(word & ((1u << bit) - 1u));
-    a = p.vals[(uint64_t)ch.owner * p.Kp + ch.base + r];
+    a = SCAPE_CHECK(p.dbg, r < ch.k, CHK_OWNER_KEY, ch.c0 + i)
+            ? p.vals[(uint64_t)ch.owner * p.Kp + ch.base + r]
+            : 0.0f;
   } else {
     a = p.e[(uint64_t)ch.owner * p.Np + ch.c0 + i];
   }
@@ -306,10 +310,10 @@ __device__ bool select_chunk(const FusedArgs& p, const Shared& sh, const Chunk& 
         uint32_t pos = 0;
         if (lane == 0 && bal) pos = atomicAdd(&sh.ctl[C_NCAND], __popc(bal));
         pos = __shfl_sync(kFull, pos, 0);
-        if (is) {
+        const uint32_t slot = pos + __popc(bal & ((1u << lane) - 1u));
+        if (is && SCAPE_CHECK(p.dbg, slot < kCap, CHK_CAND, ch.c0 + i)) {
           const uint32_t key = owner_key(p, sh, ch, i);
-          sh.cand[pos + __popc(bal & ((1u << lane) - 1u))] =
-              ((unsigned long long)key << 16) | (unsigned long long)(0xFFFFu - i);
+          sh.cand[slot] = ((unsigned long long)key << 16) | (unsigned long long)(0xFFFFu - i);
         }
       }
       __syncthreads();
@@ -453,7 +457,8 @@ __device__ __forceinline__ void update_chunk(const FusedArgs& p, const Shared& s
     const uint32_t R0 = (uint32_t)ch.base + tile0;
     for (uint32_t r0 = 0; r0 < cnt; r0 += 32) {
       float mine = 0.0f;
-      if (r0 + lane < cnt) {
+      if (r0 + lane < cnt &&
+          SCAPE_CHECK(p.dbg, tile0 + r0 + lane < ch.k, CHK_BBAR, ch.c0 + t * 256)) {
         mine = ordered_sum(p, R0 + r0 + lane) * invW;
         p.bbar[R0 + r0 + lane] = mine;
       }
@@ -484,8 +489,11 @@ __device__ __forceinline__ void update_chunk(const FusedArgs& p, const Shared& s
 #pragma unroll
     for (int jj = 0; jj < 8; jj++) {
       const bool m = (byte >> jj) & 1u;
-      if (m) p.idx[R0 + local0 - tile0 + __popc(byte & ((1u << jj) - 1u))] =
-          (uint32_t)(ch.c0 + i0 + jj);
+      if (m) {
+        const uint32_t r = local0 + __popc(byte & ((1u << jj) - 1u));
+        if (SCAPE_CHECK(p.dbg, r < ch.k, CHK_IDX, ch.c0 + i0 + jj))
+          p.idx[ch.base + r] = (uint32_t)(ch.c0 + i0 + jj);
+      }
       const float vn = (b2 * vo[jj]) + (c2 * (bb[jj] * bb[jj]));
       const float q = m ? bb[jj] / (sqrtf(vn) + eps) : 0.0f;
       vo[jj] = vn;
@@ -529,6 +537,7 @@ __global__ __launch_bounds__(kNT, 1) void step_chunks(const FusedArgs p) {
     }
     ch.nw = (ch.L + 31) / 32;
     ch.owner = (int)(c / p.q);
+    if (!SCAPE_CHECK(p.dbg, ch.c0 + ch.L <= p.N && ch.L <= kMaxChunk, CHK_CHUNK, ch.c0)) continue;
 
     // phase 0: M_{t-1} words of the chunk, their popcount prefix; clear the histogram
     {

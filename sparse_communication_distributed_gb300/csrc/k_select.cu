@@ -68,8 +68,8 @@ __device__ __forceinline__ void find_bin(SelectSmem& sm, int nb, uint32_t r) {
 // returns how many of them lie inside the chunk.
 template <int SRC>
 __device__ __forceinline__ int quad_keys(const SelectArgs& p, const SelectSmem& sm, int w,
-                                         uint64_t c0, uint32_t L, uint64_t base_c, uint32_t qd,
-                                         unsigned long long X[4]) {
+                                         uint64_t c0, uint32_t L, uint32_t kc, uint64_t base_c,
+                                         uint32_t qd, unsigned long long X[4]) {
   const uint32_t i4 = qd * 4;
   const int nv = (L - i4) >= 4 ? 4 : (int)(L - i4);
   float a[4];
@@ -84,7 +84,10 @@ __device__ __forceinline__ int quad_keys(const SelectArgs& p, const SelectSmem& 
       const uint32_t r0 = sm.wpre[j] + __popc(wb & ((1u << bit0) - 1u));
 #pragma unroll
       for (int s = 0; s < 4; s++)
-        if ((nib >> s) & 1u) a[s] = vw[r0 + __popc(nib & ((1u << s) - 1u))];
+        if ((nib >> s) & 1u) {
+          const uint32_t r = r0 + __popc(nib & ((1u << s) - 1u));
+          if (SCAPE_CHECK(p.dbg, r < kc, CHK_SELECT_VALS, c0 + i4 + s)) a[s] = vw[r];
+        }
     }
   } else {
     const float4 uv = *reinterpret_cast<const float4*>(p.u + (uint64_t)w * p.Np + c0 + i4);
@@ -179,7 +182,7 @@ __device__ void select_one(const SelectArgs& p, SelectSmem& sm, const uint64_t c
       const uint32_t qd = base + lane;
       if (qd < nq) {
         unsigned long long X[4];
-        const int nv = quad_keys<SRC>(p, sm, w, c0, L, base_c, qd, X);
+        const int nv = quad_keys<SRC>(p, sm, w, c0, L, k, base_c, qd, X);
         for (int s = 0; s < nv; s++)
           if ((X[s] >> (kTB - pbits)) == prefix)
             atomicAdd(&sm.hist[(uint32_t)(X[s] >> shift) & (uint32_t)(nb - 1)], 1u);
@@ -209,7 +212,7 @@ __device__ void select_one(const SelectArgs& p, SelectSmem& sm, const uint64_t c
     unsigned long long Xc[4];
     if (qd < nq) {
       unsigned long long X[4];
-      const int nv = quad_keys<SRC>(p, sm, w, c0, L, base_c, qd, X);
+      const int nv = quad_keys<SRC>(p, sm, w, c0, L, k, base_c, qd, X);
       for (int s = 0; s < nv; s++) {
         const unsigned long long hi = X[s] >> rem;
         if (resolved ? (hi >= prefix) : (hi > prefix)) nib |= 1u << s;

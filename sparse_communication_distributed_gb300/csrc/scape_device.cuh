@@ -7,6 +7,39 @@ namespace scape {
 
 constexpr unsigned kFull = 0xFFFFFFFFu;
 
+// Debug builds (-DSCAPE_DEBUG_CHECKS) check every index that depends on the
+// applied mask carrying exactly k_c bits per chunk.  A failed check records
+// the first failure's code and coordinate in dbg[0..3] (code, count, where
+// low, where high) and skips the access; nothing traps.  Release builds
+// compile the checks away.
+#ifdef SCAPE_DEBUG_CHECKS
+__device__ __forceinline__ bool dbg_ok(uint32_t* dbg, bool ok, uint32_t code, uint64_t where) {
+  if (!ok && dbg) {
+    if (atomicCAS(dbg, 0u, code) == 0u) {
+      dbg[2] = (uint32_t)where;
+      dbg[3] = (uint32_t)(where >> 32);
+    }
+    atomicAdd(dbg + 1, 1u);
+  }
+  return ok;
+}
+#define SCAPE_CHECK(dbg, cond, code, where) (::scape::dbg_ok((dbg), (cond), (code), (where)))
+#else
+#define SCAPE_CHECK(dbg, cond, code, where) (true)
+#endif
+
+// check codes
+enum : uint32_t {
+  CHK_VALS_WRITE = 1,   // kept value past the chunk's k
+  CHK_VALS_STAGE = 2,   // staged kept values past the chunk's k
+  CHK_BBAR = 3,         // synchronized-sum position past the chunk's k
+  CHK_IDX = 4,          // coordinate-list position past the chunk's k
+  CHK_OWNER_KEY = 5,    // kept value read past the chunk's k (selection)
+  CHK_CAND = 6,         // candidate list overflow
+  CHK_SELECT_VALS = 7,  // standalone select: kept value read past k
+  CHK_CHUNK = 8         // chunk extends past N
+};
+
 __device__ __forceinline__ uint32_t warp_incl_scan(uint32_t x, int lane) {
 #pragma unroll
   for (int d = 1; d < 32; d <<= 1) {

@@ -46,6 +46,7 @@ struct FusedArgs {
   uint32_t C, k_full, k_last;
   int W;
   int boot;  // 1: only build M_{-1} into mout from the step-0 accumulators (no writes)
+  uint32_t* dbg;  // debug builds: check-failure record (4 words), may be NULL
   float b1, c1, b2, c2, lr, wd, eps, invW;
 };
 
@@ -63,6 +64,7 @@ struct SelectArgs {
   int rank_worker;  // 0: each chunk ranks its owner's accumulator (the SCAPE rule);
                     // w + 1: every chunk ranks worker w's (mask diagnostics)
   const ChunkDesc* chunks;  // NULL: chunk c = [c*C, c*C + C) of the flat vector
+  uint32_t* dbg;            // debug builds: check-failure record (4 words), may be NULL
   uint64_t N, Np, Kp, n_ch, q;
   uint32_t C, k_full, k_last;
 };

@@ -14,6 +14,7 @@ import numpy as np
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libscape.so")
+DEBUG_LIB_PATH = os.path.join(HERE, "libscape_debug.so")
 
 SCAPE_OK, SCAPE_EINVAL, SCAPE_ENOMEM, SCAPE_ECUDA, SCAPE_ESTATE = 0, -1, -2, -3, -4
 THETA, V, U, E, MASK, STEP = 0, 1, 2, 3, 4, 5
@@ -44,7 +45,9 @@ class _Info(ctypes.Structure):
                 ("k_full", ctypes.c_uint32), ("k_last", ctypes.c_uint32), ("K", ctypes.c_uint64),
                 ("mask_words", ctypes.c_uint64), ("step", ctypes.c_int64),
                 ("device_bytes", ctypes.c_uint64), ("select_fallbacks", ctypes.c_uint64),
-                ("flags", ctypes.c_uint32), ("host_bytes", ctypes.c_uint64)]
+                ("flags", ctypes.c_uint32), ("host_bytes", ctypes.c_uint64),
+                ("checks_compiled", ctypes.c_uint32), ("check_code", ctypes.c_uint32),
+                ("check_count", ctypes.c_uint32), ("check_where", ctypes.c_uint64)]
 
 
 class StepBuffers(ctypes.Structure):
@@ -60,12 +63,16 @@ class StepBuffers(ctypes.Structure):
 
 
 _lib = None
+_libs: dict = {}
 
 
 def load_library(path: str = LIB_PATH):
+    """Load libscape (or another build of it, e.g. DEBUG_LIB_PATH) once."""
     global _lib
-    if _lib is not None:
+    if path == LIB_PATH and _lib is not None:
         return _lib
+    if path in _libs:
+        return _libs[path]
     if not os.path.exists(path):
         raise ImportError(f"{path} is missing: build it with "
                           "`python -m sparse_communication_distributed_gb300.build`")
@@ -97,7 +104,9 @@ def load_library(path: str = LIB_PATH):
     f32 = ctypes.c_float
     lib.scape_dense_adams_step.argtypes = [vp, vp, vp, ctypes.POINTER(vp), i32, u64, f32, f32, f32,
                                            f32, f32, vp]
-    _lib = lib
+    _libs[path] = lib
+    if path == LIB_PATH:
+        _lib = lib
     return lib
 
 
@@ -122,8 +131,8 @@ class Scape:
 
     def __init__(self, numel, chunk: int, W: int, density: float, beta1: float = 0.9,
                  beta2: float = 0.95, lr: float = 1e-3, wd: float = 0.1, eps: float = 1e-8,
-                 flags: int = 0):
-        self.lib = load_library()
+                 flags: int = 0, lib_path: str = LIB_PATH):
+        self.lib = load_library(lib_path)
         arr = np.ascontiguousarray(numel, dtype=np.uint64)
         lay = _Layout(arr.size, arr.ctypes.data_as(ctypes.POINTER(ctypes.c_uint64)), chunk)
         h = ctypes.c_void_p()
@@ -135,9 +144,9 @@ class Scape:
         self.info = self._info()
 
     @classmethod
-    def for_workload(cls, wl, density: float, flags: int = 0) -> "Scape":
+    def for_workload(cls, wl, density: float, flags: int = 0, lib_path: str = LIB_PATH) -> "Scape":
         return cls(wl.numel, wl.chunk, wl.W, density, wl.beta1, wl.beta2, wl.lr, wl.wd, wl.eps,
-                   flags=flags)
+                   flags=flags, lib_path=lib_path)
 
     def _check(self, rc: int) -> None:
         if rc != SCAPE_OK:
