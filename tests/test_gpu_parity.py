@@ -51,6 +51,7 @@ def test_flat_2p20_every_coordinate():
     (3000, 2, 64, 0.01),       # k = 0 everywhere
     (2048 + 7, 4, 512, 1.0),   # density 1: every coordinate, dense AdamS
     (65536 * 2 + 160, 2, 65536, 0.3),  # large k in a full chunk, 160-coordinate last chunk
+    (70001, 64, 1024, 0.05),   # the largest W
 ])
 def test_edge_shapes(N, W, chunk, density):
     wl = synth.tiny(N, W, chunk, density, seed=N)
@@ -303,3 +304,14 @@ def test_random_shapes(seed):
         check_full_mask(g, r)
     finally:
         g.close()
+
+
+def test_largest_n():
+    # N = 2^32 - 1, the largest N the uint32 coordinates allow: 65536 chunks of
+    # 65536, the last one 65535 long; W = 2 (about 120 GB on the device).
+    N = (1 << 32) - 1
+    wl = synth.Workload("max-n", (("flat", (N,)),), W=2, chunk=65536, densities=(0.001,),
+                        steps=2, sigma=1e-3, seed=90)
+    nch = -(-N // 65536)
+    ids = [0, 1, nch // 2 - 1, nch // 2, nch - 2, nch - 1]
+    _run_both(wl, 0.001, 2, chunk_ids=ids)
