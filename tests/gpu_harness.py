@@ -36,7 +36,7 @@ def assert_close_exact(name: str, got: np.ndarray, ref: np.ndarray) -> None:
                              f"first at {i}: gpu {got[i]!r} oracle {ref[i]!r}")
 
 
-class GpuRun:
+class DeviceRun:
     """libscape on a workload, inputs from the GPU build of the generator."""
 
     def __init__(self, wl, density: float, theta0: bool = True, flags: int = 0):
@@ -90,7 +90,7 @@ class OracleRun:
         self.t += 1
 
 
-def compare(g: GpuRun, r: OracleRun, what: str = "") -> None:
+def compare(g: DeviceRun, r: OracleRun, what: str = "") -> None:
     """Compare the GPU state with the oracle over the oracle's chunks."""
     if r.o.n == g.wl.N:
         return compare_all(g, r, what)
@@ -134,7 +134,7 @@ def compare(g: GpuRun, r: OracleRun, what: str = "") -> None:
         pos += ln
 
 
-def compare_all(g: GpuRun, r: OracleRun, what: str = "") -> None:
+def compare_all(g: DeviceRun, r: OracleRun, what: str = "") -> None:
     """compare() when the oracle covers every coordinate: whole arrays at once."""
     o, sc, W = r.o, g.sc, g.wl.W
     assert_close_exact(f"theta {what}", sc.read(THETA), o.get(oracle.THETA))
@@ -173,7 +173,7 @@ def sample_chunks(wl, n_extra: int = 4, seed: int = 0) -> list[int]:
 _POPC8 = np.array([bin(i).count("1") for i in range(256)], np.uint8)
 
 
-def check_full_mask(g: GpuRun, r: OracleRun | None = None) -> None:
+def check_full_mask(g: DeviceRun, r: OracleRun | None = None) -> None:
     """Properties over the full size: every chunk of the next mask carries
     exactly k_c bits, none past N; the last step's coordinate list is strictly
     increasing and has K entries.  Chunk boundaries come from the oracle's

@@ -10,7 +10,7 @@ if not torch.cuda.is_available():
     pytest.skip("needs a CUDA GPU", allow_module_level=True)
 
 import synth  # noqa: E402
-from gpu_harness import GpuRun  # noqa: E402
+from gpu_harness import DeviceRun  # noqa: E402
 from sparse_communication_distributed_gb300 import MASK, STEP, THETA, Scape, ScapeError  # noqa: E402
 from sparse_communication_distributed_gb300.scape import (SCAPE_EINVAL, SCAPE_ENOMEM,  # noqa: E402
                                                           SCAPE_ESTATE)
@@ -51,7 +51,7 @@ def test_calls_before_the_first_step():
 
 def test_bad_step_arguments_leave_the_handle_usable():
     wl = synth.tiny(8192, 2, 1024, 0.1)
-    g = GpuRun(wl, 0.1)
+    g = DeviceRun(wl, 0.1)
     try:
         buf = torch.empty(wl.N + 8, dtype=torch.int16, device="cuda")
         with pytest.raises(ScapeError) as ei:
@@ -69,7 +69,7 @@ def test_bad_step_arguments_leave_the_handle_usable():
 
 def test_mask_load_is_validated_and_used():
     wl = synth.tiny(4096 + 64, 2, 1024, 0.05)  # k = 51 per full chunk, 3 in the last
-    g = GpuRun(wl, 0.05)
+    g = DeviceRun(wl, 0.05)
     try:
         words = np.zeros(g.sc.info["mask_words"], np.uint32)
         with pytest.raises(ScapeError) as ei:

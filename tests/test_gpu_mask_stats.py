@@ -10,7 +10,7 @@ if not torch.cuda.is_available():
 
 import oracle  # noqa: E402
 import synth  # noqa: E402
-from gpu_harness import GpuRun, OracleRun, compare  # noqa: E402
+from gpu_harness import DeviceRun, OracleRun, compare  # noqa: E402
 
 pytestmark = pytest.mark.gpu
 
@@ -18,7 +18,7 @@ pytestmark = pytest.mark.gpu
 @pytest.mark.parametrize("W,kind", [(3, synth.SYN_GAUSS), (4, synth.SYN_STUDENT_Q)])
 def test_mask_stats_match_oracle(W, kind):
     wl = synth.tiny(6 * 1024 + 352, W, 1024, 0.1, kind=kind, seed=50 + W)
-    g, r = GpuRun(wl, 0.1), OracleRun(wl, 0.1)
+    g, r = DeviceRun(wl, 0.1), OracleRun(wl, 0.1)
     try:
         for t in range(4):
             g.step()

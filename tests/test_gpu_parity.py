@@ -19,14 +19,14 @@ if not torch.cuda.is_available():
 
 import oracle  # noqa: E402
 import synth  # noqa: E402
-from gpu_harness import GpuRun, OracleRun, check_full_mask, compare, sample_chunks  # noqa: E402
+from gpu_harness import DeviceRun, OracleRun, check_full_mask, compare, sample_chunks  # noqa: E402
 from sparse_communication_distributed_gb300 import E, MASK, STEP, THETA, U, V, Scape  # noqa: E402
 
 pytestmark = pytest.mark.gpu
 
 
 def _run_both(wl, density, steps, chunk_ids=None, every=True):
-    g = GpuRun(wl, density)
+    g = DeviceRun(wl, density)
     r = OracleRun(wl, density, chunk_ids=chunk_ids)
     try:
         for t in range(steps):
@@ -73,7 +73,7 @@ def _const_grads(wl, value):
 def test_all_equal_accumulators():
     # constant gradient: every |a| in a chunk is equal, the first k coordinates win
     wl = synth.tiny(8192 + 96, 2, 4096, 0.1)
-    g, r = GpuRun(wl, 0.1), OracleRun(wl, 0.1)
+    g, r = DeviceRun(wl, 0.1), OracleRun(wl, 0.1)
     try:
         for t in range(3):
             gr = _const_grads(wl, -0.0625)
@@ -97,7 +97,7 @@ def test_loaded_residuals_select_exactly():
     e0 = (rng.integers(-8, 9, (2, wl.N)) * 0.5).astype(np.float32)
     e0[:, ::97] = -0.0
     e0[:, 5::131] = np.float32(1e-40)
-    g, r = GpuRun(wl, 0.25), OracleRun(wl, 0.25)
+    g, r = DeviceRun(wl, 0.25), OracleRun(wl, 0.25)
     try:
         for w in range(2):
             g.sc.load(E, e0[w], w)
@@ -127,7 +127,7 @@ def test_tied_bucket_paths(n_high, n_tied, expect_fallback):
             pos = c * 65536 + rng.permutation(65536)[: n_high + n_tied]
             e0[w, pos[:n_high]] = 2.0
             e0[w, pos[n_high:]] = -1.0
-    g, r = GpuRun(wl, 0.01), OracleRun(wl, 0.01)
+    g, r = DeviceRun(wl, 0.01), OracleRun(wl, 0.01)
     try:
         for w in range(2):
             g.sc.load(E, e0[w], w)
@@ -143,19 +143,19 @@ def test_tied_bucket_paths(n_high, n_tied, expect_fallback):
 
 def test_resume_is_bit_identical():
     wl = synth.tiny(3 * 4096 + 32, 3, 4096, 0.05, seed=8)
-    a = GpuRun(wl, 0.05)
+    a = DeviceRun(wl, 0.05)
     for _ in range(5):
         a.step()
     ref = {f: a.sc.read(f) for f in (THETA, V, MASK)}
     ref_u = [a.sc.read(U, w) for w in range(3)]
     a.close()
-    b = GpuRun(wl, 0.05)
+    b = DeviceRun(wl, 0.05)
     for _ in range(3):
         b.step()
     saved = {f: b.sc.read(f) for f in (THETA, V, MASK, STEP)}
     saved_ue = [(b.sc.read(U, w), b.sc.read(E, w)) for w in range(3)]
     b.close()
-    c = GpuRun(wl, 0.05, theta0=False)
+    c = DeviceRun(wl, 0.05, theta0=False)
     for f in (THETA, V, MASK, STEP):
         c.sc.load(f, saved[f])
     for w in range(3):
@@ -178,7 +178,7 @@ def test_resume_is_bit_identical():
 def test_step_host_matches_step(memory):
     # pinned buffers are read in place by the kernel; pageable ones are staged
     wl = synth.tiny(20000, 2, 1024, 0.1, seed=4)
-    a, b = GpuRun(wl, 0.1), GpuRun(wl, 0.1)
+    a, b = DeviceRun(wl, 0.1), DeviceRun(wl, 0.1)
     try:
         for t in range(3):
             gr = np.stack([synth.cpu().grads(wl, w, t, n=wl.N) for w in range(2)])
@@ -228,7 +228,7 @@ from sparse_communication_distributed_gb300.scape import CHUNK_PER_TENSOR, RESID
 
 
 def _per_tensor_run(wl, density, steps, chunk_ids=None):
-    g = GpuRun(wl, density, flags=CHUNK_PER_TENSOR)
+    g = DeviceRun(wl, density, flags=CHUNK_PER_TENSOR)
     r = OracleRun(wl, density, chunk_ids=chunk_ids, per_tensor=True)
     try:
         assert g.sc.info["n_chunks"] == r.o.all_chunks()[0].size
@@ -265,7 +265,7 @@ def test_per_tensor_gpt2_full_size_sampled():
 
 def test_residuals_in_host_memory():
     wl = synth.tiny(3 * 4096 + 200, 3, 4096, 0.05, seed=61)
-    g, r = GpuRun(wl, 0.05, flags=RESIDUAL_HOST), OracleRun(wl, 0.05)
+    g, r = DeviceRun(wl, 0.05, flags=RESIDUAL_HOST), OracleRun(wl, 0.05)
     try:
         assert g.sc.info["host_bytes"] >= 3 * wl.N * 4
         for t in range(3):
@@ -294,7 +294,7 @@ def _random_case(seed):
 @pytest.mark.parametrize("seed", range(12))
 def test_random_shapes(seed):
     wl, density, per_tensor = _random_case(seed)
-    g = GpuRun(wl, density, flags=CHUNK_PER_TENSOR if per_tensor else 0)
+    g = DeviceRun(wl, density, flags=CHUNK_PER_TENSOR if per_tensor else 0)
     r = OracleRun(wl, density, per_tensor=per_tensor)
     try:
         for t in range(3):

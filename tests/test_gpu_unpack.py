@@ -10,7 +10,7 @@ if not torch.cuda.is_available():
 
 import oracle  # noqa: E402
 import synth  # noqa: E402
-from gpu_harness import GpuRun, OracleRun, assert_close_exact  # noqa: E402
+from gpu_harness import DeviceRun, OracleRun, assert_close_exact  # noqa: E402
 from sparse_communication_distributed_gb300.scape import unpack  # noqa: E402
 
 pytestmark = pytest.mark.gpu
@@ -18,7 +18,7 @@ pytestmark = pytest.mark.gpu
 
 def test_pack_unpack_round_trip():
     wl = synth.tiny(5 * 4096 + 160, 3, 4096, 0.07, seed=71)
-    g, r = GpuRun(wl, 0.07), OracleRun(wl, 0.07)
+    g, r = DeviceRun(wl, 0.07), OracleRun(wl, 0.07)
     dev = torch.device("cuda")
     try:
         for t in range(3):
