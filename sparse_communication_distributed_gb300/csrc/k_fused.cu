@@ -573,6 +573,7 @@ __global__ __launch_bounds__(kNT, 1) void step_chunks(const FusedArgs p) {
       } else if (tid == 0) {
         p.fallback[c] = 1u;
         atomicAdd(p.n_fallback, 1u);
+        if (p.pending) atomicAdd(p.pending, 1u);
       }
       __syncthreads();
       continue;
@@ -591,6 +592,7 @@ __global__ __launch_bounds__(kNT, 1) void step_chunks(const FusedArgs p) {
     } else if (tid == 0) {
       p.fallback[c] = 1u;
       atomicAdd(p.n_fallback, 1u);
+      if (p.pending) atomicAdd(p.pending, 1u);
     }
 
     // phase 3: every other worker

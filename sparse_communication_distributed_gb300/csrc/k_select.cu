@@ -276,6 +276,7 @@ __device__ void select_one(const SelectArgs& p, SelectSmem& sm, const uint64_t c
 template <int SRC>
 __global__ __launch_bounds__(kNT, 2) void select_topk(const SelectArgs p) {
   __shared__ SelectSmem sm;
+  if (p.pending && *p.pending == 0u) return;  // the step kernel flagged no chunk
   for (uint64_t c = blockIdx.x; c < p.n_ch; c += gridDim.x) {
     if (p.flags && p.flags[c] == 0u) continue;
     select_one<SRC>(p, sm, c);

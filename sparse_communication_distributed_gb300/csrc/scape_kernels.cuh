@@ -41,6 +41,7 @@ struct FusedArgs {
   uint32_t* mout;
   uint32_t* fallback;    // per chunk: 1 = selection left to the standalone select
   uint32_t* n_fallback;  // count of such chunks (diagnostic)
+  uint32_t* pending;     // chunks flagged by this launch (zeroed before it; may be NULL)
   const ChunkDesc* chunks;  // NULL: chunk c = [c*C, c*C + C) of the flat vector
   uint64_t N, Np, Kp, n_ch, q;
   uint32_t C, k_full, k_last;
@@ -61,6 +62,7 @@ struct SelectArgs {
   float b1, c1;
   uint32_t* mout;
   uint32_t* flags;  // NULL: every chunk; else only chunks with flags[c] != 0 (cleared)
+  const uint32_t* pending;  // if set and zero, no chunk is flagged: the launch returns at once
   int rank_worker;  // 0: each chunk ranks its owner's accumulator (the SCAPE rule);
                     // w + 1: every chunk ranks worker w's (mask diagnostics)
   const ChunkDesc* chunks;  // NULL: chunk c = [c*C, c*C + C) of the flat vector
