@@ -315,3 +315,31 @@ def test_largest_n():
     nch = -(-N // 65536)
     ids = [0, 1, nch // 2 - 1, nch // 2, nch - 2, nch - 1]
     _run_both(wl, 0.001, 2, chunk_ids=ids)
+
+
+def test_per_tensor_with_host_residuals_and_mask_stats():
+    # both options at once, and the mask diagnostics on per-tensor chunks
+    numel = [96, 20000 * 32, 64, 4096 + 33]
+    wl = synth.Workload("pt-host", tuple((f"t{i}", (n,)) for i, n in enumerate(numel)), W=3,
+                        chunk=2048, densities=(0.05,), steps=3, sigma=1e-3, seed=62)
+    g = DeviceRun(wl, 0.05, flags=CHUNK_PER_TENSOR | RESIDUAL_HOST)
+    r = OracleRun(wl, 0.05, per_tensor=True)
+    try:
+        for t in range(3):
+            g.step()
+            r.step()
+            compare(g, r, f"step {t}")
+        st = g.sc.mask_stats()
+        o = r.o
+        m_new, m_used = o.mask(0).astype(bool), o.mask(1).astype(bool)
+        union = np.zeros(o.n, bool)
+        for w in range(wl.W):
+            a = o.get(oracle.A, w)
+            for j in range(o.chunk_start.size):
+                s0, ln, k = int(o.chunk_start[j]), int(o.chunk_len[j]), int(o.chunk_k[j])
+                union[s0:s0 + ln] |= oracle.topk(a[s0:s0 + ln], k).astype(bool)
+        assert st["kept"] == int(m_new.sum())
+        assert st["overlap_prev"] == int((m_new & m_used).sum())
+        assert st["union_global_topk"] == int(union.sum())
+    finally:
+        g.close()
