@@ -222,6 +222,34 @@ def run_reference(args, wl, density):
     print(json.dumps(line), flush=True)
 
 
+def link_duplex_gbs(dev, nbytes=1 << 30, reps=3):
+    """Host-link ceiling for state kept in host memory: one page-locked buffer
+    copied to the device while another comes back, on two streams at once
+    (bytes of both directions / time, best of `reps`)."""
+    import torch
+    h_in = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    h_out = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    d_in = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    d_out = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
+    s1, s2 = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    best = 0.0
+    for _ in range(reps):
+        torch.cuda.synchronize(dev)
+        a, b, c = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        a.record(s1)
+        s2.wait_event(a)
+        with torch.cuda.stream(s1):
+            d_in.copy_(h_in, non_blocking=True)
+        with torch.cuda.stream(s2):
+            h_out.copy_(d_out, non_blocking=True)
+        c.record(s2)
+        s1.wait_event(c)
+        b.record(s1)
+        torch.cuda.synchronize(dev)
+        best = max(best, 2 * nbytes / (a.elapsed_time(b) * 1e-3) / 1e9)
+    return best
+
+
 def run_scape(args, wl, density):
     import torch
     from sparse_communication_distributed_gb300 import THETA, Scape
@@ -365,6 +393,15 @@ def run_scape(args, wl, density):
                          f"{n_st} steps incl. step 0 over 2 gradient batches, {dt:.1f} s of "
                          f"oracle time; single-threaded C++ oracle on one host core"}
 
+    link = None
+    if args.residual_host:
+        duplex = link_duplex_gbs(dev)
+        rb = 8.0 * W * N  # every residual read and written once per step
+        link = {"residual_bytes_per_step": rb,
+                "achieved_gbs": rb / (ms_per_step * 1e-3) / 1e9,
+                "duplex_copy_gbs": duplex,
+                "frac": rb / (ms_per_step * 1e-3) / 1e9 / duplex,
+                "peak_kind": "measured here: concurrent page-locked copies in both directions"}
     if rank != 0:
         ranks.close()
         return
@@ -409,6 +446,7 @@ def run_scape(args, wl, density):
         "select_fallback_chunks": sc._info()["select_fallbacks"],
         "clocks": clk,
         "e2e": e2e,
+        "residual_link": link,
         "dense_adams": dense,
         "mask_stats": mstats,
         "cpu_baseline": cpu,

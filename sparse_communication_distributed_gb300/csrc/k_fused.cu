@@ -222,6 +222,117 @@ __device__ __forceinline__ void stream_worker(const FusedArgs& p, const Shared& 
   }
 }
 
+// The same pass for residuals held in mapped host memory.  Each lane takes two
+// groups of 4 consecutive coordinates, 128 apart, one group after the other,
+// so that every warp access of u and e covers 512 contiguous bytes.  Over the
+// CPU-GPU link an access that covers half of each 32-byte sector (the layout
+// above) moves half the useful bytes per transfer; in HBM, L2 merges the
+// halves and the layout above, with twice the bytes in flight per thread, is
+// faster.
+template <int PASS>
+__device__ __forceinline__ void stream_worker_contig(const FusedArgs& p, const Shared& sh,
+                                              const Chunk& ch, int w) {
+  constexpr bool KEYS = PASS != PASS_OTHER;
+  constexpr bool WRITE = PASS != PASS_BOOT;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint16_t* __restrict__ g = p.grads[w] + ch.c0;
+  float* __restrict__ u = p.u + (uint64_t)w * p.Np + ch.c0;
+  float* __restrict__ e = p.e + (uint64_t)w * p.Np + ch.c0;
+  float* __restrict__ vals = p.vals + (uint64_t)w * p.Kp + ch.base;
+  const float b1 = p.b1, c1 = p.c1;
+  float* stage = sh.stage + warp * 32;
+  const uint32_t ntile = (ch.L + 255) / 256;
+  const uint32_t sft = (lane & 7) * 4;  // the group's nibble in its mask word
+  for (uint32_t t = warp; t < ntile; t += kNW) {  // warp-uniform: every lane takes part
+    const uint32_t tile0 = WRITE ? (uint32_t)sh.wpre[t * 8] : 0u;  // first kept value's rank
+    const uint32_t ia = t * 256 + lane * 4;  // group h starts at ia + 128 h
+    uint32_t nr[2] = {0u, 0u};  // group h: mask nibble << 28 | rank of its first coordinate
+    uint2 gr[2];
+    float4 uv[2], ev[2];
+#pragma unroll
+    for (int h = 0; h < 2; h++) {
+      const uint32_t i0 = ia + h * 128;
+      if (WRITE && i0 < ch.L) {
+        const uint32_t j = i0 >> 5;
+        const uint32_t word = sh.wprev[j];
+        nr[h] = (((word >> sft) & 0xFu) << 28) | (sh.wpre[j] + __popc(word & ((1u << sft) - 1u)));
+      }
+    }
+    // kept value of element jj of group h: tile rank < 32 -> staged, else stored directly
+#define SCAPE_KEEP(h, jj, bval)                                                     \
+    do {                                                                            \
+      const uint32_t r_ = (nr[h] & 0x0FFFFFFFu) + __popc((nr[h] >> 28) & ((1u << (jj)) - 1u)); \
+      if (r_ - tile0 < 32u) stage[r_ - tile0] = (bval);                             \
+      else if (SCAPE_CHECK(p.dbg, r_ < ch.k, CHK_VALS_WRITE,                        \
+                           ch.c0 + ia + (h) * 128 + (jj))) vals[r_] = (bval);       \
+    } while (0)
+#pragma unroll
+    for (int h = 0; h < 2; h++) {
+      const uint32_t i0 = ia + h * 128;
+      if (i0 + 4 <= ch.L) {
+        gr[h] = ld_stream_u2(g + i0);
+        uv[h] = *reinterpret_cast<const float4*>(u + i0);
+        ev[h] = *reinterpret_cast<const float4*>(e + i0);
+        float gf[4] = {bf16lo(gr[h].x), bf16hi(gr[h].x), bf16lo(gr[h].y), bf16hi(gr[h].y)};
+        float uu[4] = {uv[h].x, uv[h].y, uv[h].z, uv[h].w};
+        float ee[4] = {ev[h].x, ev[h].y, ev[h].z, ev[h].w};
+        uint32_t k16[4];
+#pragma unroll
+        for (int jj = 0; jj < 4; jj++) {
+          const float un = (b1 * uu[jj]) + (c1 * gf[jj]);
+          const float a = ee[jj] + un;
+          if (WRITE) {
+            const bool m = (nr[h] >> (28 + jj)) & 1u;
+            const float b = m ? a : 0.0f;
+            uu[jj] = un;
+            ee[jj] = a - b;
+            if (m) SCAPE_KEEP(h, jj, b);
+          }
+          if (KEYS) {
+            const uint32_t key = __float_as_uint(a) & 0x7FFFFFFFu;
+            k16[jj] = key >> 15;
+            atomicAdd(&sh.hist[key >> 19], 1u);
+          }
+        }
+        if (WRITE) {
+          *reinterpret_cast<float4*>(u + i0) = make_float4(uu[0], uu[1], uu[2], uu[3]);
+          *reinterpret_cast<float4*>(e + i0) = make_float4(ee[0], ee[1], ee[2], ee[3]);
+        }
+        if (KEYS)
+          *reinterpret_cast<uint2*>(sh.key16 + i0) =
+              make_uint2(k16[0] | (k16[1] << 16), k16[2] | (k16[3] << 16));
+      } else if (i0 < ch.L) {  // the chunk's ragged end
+        const uint32_t nv = ch.L - i0;
+        for (uint32_t jj = 0; jj < nv; jj++) {
+          const uint32_t i = i0 + jj;
+          const float un = (b1 * u[i]) + (c1 * bf16f(g[i]));
+          const float a = e[i] + un;
+          if (WRITE) {
+            const bool m = (nr[h] >> (28 + jj)) & 1u;
+            const float b = m ? a : 0.0f;
+            u[i] = un;
+            e[i] = a - b;
+            if (m) SCAPE_KEEP(h, jj, b);
+          }
+          if (KEYS) {
+            const uint32_t key = __float_as_uint(a) & 0x7FFFFFFFu;
+            sh.key16[i] = (uint16_t)(key >> 15);
+            atomicAdd(&sh.hist[key >> 19], 1u);
+          }
+        }
+      }
+    }
+#undef SCAPE_KEEP
+    if (WRITE) {
+      const uint32_t cnt = __reduce_add_sync(kFull, (uint32_t)(__popc(nr[0] >> 28) + __popc(nr[1] >> 28)));
+      __syncwarp();
+      if (lane < cnt && SCAPE_CHECK(p.dbg, tile0 + lane < ch.k, CHK_VALS_STAGE, ch.c0 + t * 256))
+        vals[tile0 + lane] = stage[lane];
+      __syncwarp();
+    }
+  }
+}
+
 // Full 31-bit key of the owner's accumulator at chunk coordinate i, rebuilt
 // from what phase 1 wrote: the kept value on M_{t-1}, else the residual (or,
 // in the step-0 pass, recomputed from the untouched state and gradient).
@@ -515,6 +626,15 @@ __device__ __forceinline__ void update_chunk(const FusedArgs& p, const Shared& s
   }
 }
 
+template <int PASS, bool CONTIG>
+__device__ __forceinline__ void stream_pass(const FusedArgs& p, const Shared& sh, const Chunk& ch,
+                                            int w) {
+  if (CONTIG) stream_worker_contig<PASS>(p, sh, ch, w);
+  else stream_worker<PASS>(p, sh, ch, w);
+}
+
+// CONTIG: residual rows in mapped host memory (whole-sector access mapping)
+template <bool CONTIG>
 __global__ __launch_bounds__(kNT, 1) void step_chunks(const FusedArgs p) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   const Shared sh = carve(smem_raw);
@@ -564,7 +684,7 @@ __global__ __launch_bounds__(kNT, 1) void step_chunks(const FusedArgs p) {
     if (p.boot) {
       // step 0, first launch: M_{-1} of this chunk from the owner's step-0
       // accumulator (read only), ranked on chip like M_t below
-      stream_worker<PASS_BOOT>(p, sh, ch, ch.owner);
+      stream_pass<PASS_BOOT, CONTIG>(p, sh, ch, ch.owner);
       __syncthreads();
       const bool ok = select_chunk(p, sh, ch);
       if (ok) {
@@ -580,7 +700,7 @@ __global__ __launch_bounds__(kNT, 1) void step_chunks(const FusedArgs p) {
     }
 
     // phase 1: the owner's pass, keeping its keys
-    stream_worker<PASS_OWNER>(p, sh, ch, ch.owner);
+    stream_pass<PASS_OWNER, CONTIG>(p, sh, ch, ch.owner);
     if (p.W > 1) prefetch_worker_tile(p, ch.c0, ch.L, ch.owner == 0 ? 1 : 0);
     __syncthreads();
 
@@ -597,7 +717,7 @@ __global__ __launch_bounds__(kNT, 1) void step_chunks(const FusedArgs p) {
 
     // phase 3: every other worker
     for (int w = 0; w < p.W; w++)
-      if (w != ch.owner) stream_worker<PASS_OTHER>(p, sh, ch, w);
+      if (w != ch.owner) stream_pass<PASS_OTHER, CONTIG>(p, sh, ch, w);
     {
       const uint32_t i0 = (tid >> 5) * 256 + (tid & 31) * 8;
       if (i0 + 8 <= ch.L) {
@@ -625,16 +745,21 @@ __global__ __launch_bounds__(kNT, 1) void step_chunks(const FusedArgs p) {
 }  // namespace
 
 cudaError_t launch_step_chunks(const FusedArgs& a, cudaStream_t s) {
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(step_chunks, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  static bool configured[2] = {false, false};
+  const int contig = a.e_host ? 1 : 0;
+  if (!configured[contig]) {
+    cudaError_t e = cudaFuncSetAttribute(contig ? step_chunks<true> : step_chunks<false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kSmemBytes);
     if (e != cudaSuccess) return e;
-    configured = true;
+    configured[contig] = true;
   }
   uint64_t grid = (uint64_t)num_sms();
   if (grid > a.n_ch) grid = a.n_ch;
-  step_chunks<<<(unsigned)grid, kNT, kSmemBytes, s>>>(a);
+  if (contig)
+    step_chunks<true><<<(unsigned)grid, kNT, kSmemBytes, s>>>(a);
+  else
+    step_chunks<false><<<(unsigned)grid, kNT, kSmemBytes, s>>>(a);
   return cudaGetLastError();
 }
 

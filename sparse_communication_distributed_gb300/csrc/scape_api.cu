@@ -413,6 +413,7 @@ static void fill_fused(const scape_handle* h, const uint16_t* const* g, const ui
   a.k_last = h->k_last;
   a.W = h->W;
   a.boot = 0;
+  a.e_host = (h->flags & SCAPE_RESIDUAL_HOST) ? 1 : 0;
   a.b1 = h->b1;
   a.c1 = h->c1;
   a.b2 = h->b2;

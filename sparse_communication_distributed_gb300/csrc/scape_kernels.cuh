@@ -47,6 +47,7 @@ struct FusedArgs {
   uint32_t C, k_full, k_last;
   int W;
   int boot;  // 1: only build M_{-1} into mout from the step-0 accumulators (no writes)
+  int e_host;  // 1: e lives in mapped host memory (whole-sector access mapping)
   uint32_t* dbg;  // debug builds: check-failure record (4 words), may be NULL
   float b1, c1, b2, c2, lr, wd, eps, invW;
 };

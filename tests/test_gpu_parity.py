@@ -306,6 +306,24 @@ def test_random_shapes(seed):
         g.close()
 
 
+@pytest.mark.parametrize("seed", range(12, 18))
+def test_random_shapes_host_residuals(seed):
+    # the whole-sector access mapping of residuals in host memory, on ragged
+    # chunk ends of every residue mod 4 and W from 1 to 9
+    wl, density, per_tensor = _random_case(seed)
+    flags = RESIDUAL_HOST | (CHUNK_PER_TENSOR if per_tensor else 0)
+    g = DeviceRun(wl, density, flags=flags)
+    r = OracleRun(wl, density, per_tensor=per_tensor)
+    try:
+        for t in range(3):
+            g.step()
+            r.step()
+            compare(g, r, f"seed {seed} step {t}")
+        check_full_mask(g, r)
+    finally:
+        g.close()
+
+
 def test_largest_n():
     # N = 2^32 - 1, the largest N the uint32 coordinates allow: 65536 chunks of
     # 65536, the last one 65535 long; W = 2 (about 120 GB on the device).
