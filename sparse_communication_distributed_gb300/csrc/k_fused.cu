@@ -43,6 +43,7 @@
 // Per coordinate the HBM traffic is W*(2 g + 8 u + 8 e + 1/8 mask) + 8 theta +
 // 8 v + 1/8 new mask bytes, plus 4 B per kept value per worker written and
 // read back and 8 B per kept coordinate (bbar, idx) -- the compulsory bytes.
+#include <atomic>
 #include "scape_device.cuh"
 #include "scape_kernels.cuh"
 
@@ -745,14 +746,18 @@ __global__ __launch_bounds__(kNT, 1) void step_chunks(const FusedArgs p) {
 }  // namespace
 
 cudaError_t launch_step_chunks(const FusedArgs& a, cudaStream_t s) {
-  static bool configured[2] = {false, false};
+  // the shared-memory opt-in is per device and per instantiation
+  static std::atomic<uint64_t> configured[2];
   const int contig = a.e_host ? 1 : 0;
-  if (!configured[contig]) {
-    cudaError_t e = cudaFuncSetAttribute(contig ? step_chunks<true> : step_chunks<false>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kSmemBytes);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = dev < 64 ? (1ull << dev) : 0ull;  // devices past 64: set every launch
+  if (!(configured[contig].load() & bit)) {
+    e = cudaFuncSetAttribute(contig ? step_chunks<true> : step_chunks<false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess) return e;
-    configured[contig] = true;
+    configured[contig].fetch_or(bit);
   }
   uint64_t grid = (uint64_t)num_sms();
   if (grid > a.n_ch) grid = a.n_ch;
