@@ -158,6 +158,19 @@ int scape_step_host(scape_handle* h, const void* const* host_grad_ptrs, void* st
  * SCAPE_ESTATE before the first step (unless a mask was loaded). */
 int scape_mask(scape_handle* h, uint32_t* out_bits);
 
+/* Stream-ordered copy of M_t into out_bits (mask_words uint32, host or
+ * device; page-locked host memory lets the copy overlap other work).  The
+ * copy is enqueued on "stream" after everything already enqueued on the last
+ * step's stream, and the call returns at once.  out_bits is written when
+ * "stream" reaches the copy and must stay valid until then.  Later steps may
+ * be enqueued at once: a step that would overwrite the buffer being read
+ * (every second step reuses it) first waits, on the GPU, for the copy; the
+ * synchronous readers, scape_load_state and scape_destroy wait for it on the
+ * host.  So the read-back of step t's mask runs while step t+1 runs.
+ * SCAPE_ESTATE before the first step (unless a mask was loaded); CUDA
+ * failures give SCAPE_ECUDA. */
+int scape_mask_async(scape_handle* h, uint32_t* out_bits, void* stream);
+
 /* Free everything the handle owns (waits for its last step). NULL is a no-op. */
 void scape_destroy(scape_handle* h);
 

@@ -68,6 +68,10 @@ struct scape_handle {
   uint64_t device_bytes = 0;
   // profiling
   bool profiling = false;
+  // scape_mask_async: per mask buffer, the event after its last enqueued read
+  // and whether a step must still wait for it before overwriting the buffer
+  cudaEvent_t ev_written = nullptr, ev_read[2] = {nullptr, nullptr};
+  bool read_pending[2] = {false, false};
   std::vector<cudaEvent_t> ev_pool;
   std::vector<std::pair<int, std::pair<cudaEvent_t, cudaEvent_t>>> ev_rec;
   std::string err;
@@ -121,6 +125,8 @@ void release(scape_handle* h) {
     if (h->flags & SCAPE_RESIDUAL_HOST) cudaFreeHost(h->e);
     else cudaFree(h->e);
   }
+  for (cudaEvent_t ev : {h->ev_written, h->ev_read[0], h->ev_read[1]})
+    if (ev) cudaEventDestroy(ev);
   for (cudaEvent_t ev : h->ev_pool) cudaEventDestroy(ev);
   for (auto& r : h->ev_rec) {
     cudaEventDestroy(r.second.first);
@@ -163,8 +169,15 @@ struct PhaseTimer {
 
 bool is_field(int which) { return which >= SCAPE_THETA && which <= SCAPE_STEP; }
 
+// Waits for the last step and for every mask read still in flight.
 cudaError_t wait_last(scape_handle* h) {
-  return h->last_stream ? cudaStreamSynchronize(h->last_stream) : cudaDeviceSynchronize();
+  cudaError_t e = h->last_stream ? cudaStreamSynchronize(h->last_stream) : cudaDeviceSynchronize();
+  for (int b = 0; b < 2 && e == cudaSuccess; b++)
+    if (h->read_pending[b]) {
+      e = cudaEventSynchronize(h->ev_read[b]);
+      if (e == cudaSuccess) h->read_pending[b] = false;
+    }
+  return e;
 }
 
 // Checks that a 0/1 bitmap (host copy) carries exactly k_c bits in every chunk
@@ -447,6 +460,17 @@ static int step_device(scape_handle* h, const uint16_t* const* g, cudaStream_t s
   sa.chunks = h->chunks_dev;
   sa.dbg = h->dbg;
 
+  // a mask read enqueued by scape_mask_async on another stream must finish
+  // before this step overwrites its buffer (M_t here; M_{-1} too at step 0)
+  for (int b = 0; b < 2; b++) {
+    const bool written = b == 1 - h->prev || !h->has_mask;
+    if (written && h->read_pending[b]) {
+      if ((e = cudaStreamWaitEvent(s, h->ev_read[b], 0)) != cudaSuccess)
+        return cuda_fail(h, e, "wait for a mask read");
+      h->read_pending[b] = false;
+    }
+  }
+
   FusedArgs a{};
   if (!h->has_mask) {  // step 0: M_{-1} from the step-0 accumulators
     PhaseTimer pt(h, SCAPE_PH_SELECT_BOOT, s);
@@ -568,6 +592,29 @@ SCAPE_API int scape_mask(scape_handle* h, uint32_t* out_bits) {
   if (e == cudaSuccess)
     e = cudaMemcpy(out_bits, h->mask[h->prev], h->mask_words * 4, cudaMemcpyDefault);
   return e == cudaSuccess ? SCAPE_OK : cuda_fail(h, e, "scape_mask");
+}
+
+SCAPE_API int scape_mask_async(scape_handle* h, uint32_t* out_bits, void* stream) {
+  if (!h) return SCAPE_EINVAL;
+  if (!out_bits) return fail(h, SCAPE_EINVAL, "out_bits is NULL");
+  if (!h->has_mask) return fail(h, SCAPE_ESTATE, "no mask before the first step");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaSuccess;
+  if (!h->ev_written) e = cudaEventCreateWithFlags(&h->ev_written, cudaEventDisableTiming);
+  for (int b = 0; b < 2 && e == cudaSuccess; b++)
+    if (!h->ev_read[b]) e = cudaEventCreateWithFlags(&h->ev_read[b], cudaEventDisableTiming);
+  const int b = h->prev;  // M_t
+  // the copy starts after everything enqueued so far on the last step's stream
+  if (e == cudaSuccess && s != h->last_stream) {
+    e = cudaEventRecord(h->ev_written, h->last_stream);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, h->ev_written, 0);
+  }
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(out_bits, h->mask[b], h->mask_words * 4, cudaMemcpyDefault, s);
+  if (e == cudaSuccess) e = cudaEventRecord(h->ev_read[b], s);
+  if (e != cudaSuccess) return cuda_fail(h, e, "scape_mask_async");
+  h->read_pending[b] = true;
+  return SCAPE_OK;
 }
 
 static int field_ptr(scape_handle* h, int which, int w, char** base, uint64_t* count,

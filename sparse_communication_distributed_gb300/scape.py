@@ -22,7 +22,8 @@ PHASES = ("select_boot", "step", "select_fallback", "h2d")
 
 # Symbols declared in include/scape.h (checked by the ABI test).
 CHUNK_PER_TENSOR, RESIDUAL_HOST = 1, 2
-EXPORTS = ("scape_create", "scape_create_ex", "scape_step", "scape_step_host", "scape_mask", "scape_destroy",
+EXPORTS = ("scape_create", "scape_create_ex", "scape_step", "scape_step_host", "scape_mask",
+           "scape_mask_async", "scape_destroy",
            "scape_info", "scape_read_state", "scape_load_state", "scape_read_sparse",
            "scape_last_error", "scape_profile", "scape_profile_read", "scape_step_noalloc",
            "scape_dense_adams_step", "scape_mask_stats", "scape_unpack")
@@ -87,6 +88,7 @@ def load_library(path: str = LIB_PATH):
     lib.scape_step.argtypes = [vp, ctypes.POINTER(vp), vp]
     lib.scape_step_host.argtypes = [vp, ctypes.POINTER(vp), vp]
     lib.scape_mask.argtypes = [vp, vp]
+    lib.scape_mask_async.argtypes = [vp, vp, vp]
     lib.scape_destroy.argtypes = [vp]
     lib.scape_destroy.restype = None
     lib.scape_info.argtypes = [vp, ctypes.POINTER(_Info)]
@@ -192,6 +194,11 @@ class Scape:
 
     def mask_into(self, out) -> None:
         self._check(self.lib.scape_mask(self.h, _ptr(out)))
+
+    def mask_into_async(self, out, stream) -> None:
+        """Stream-ordered copy of M_t into out (pinned host or device tensor of
+        mask_words int32); out is written when `stream` reaches the copy."""
+        self._check(self.lib.scape_mask_async(self.h, _ptr(out), _stream_handle(stream)))
 
     def mask(self) -> np.ndarray:
         out = np.empty(self.info["mask_words"], np.uint32)
