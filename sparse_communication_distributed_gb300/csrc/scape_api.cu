@@ -234,6 +234,7 @@ SCAPE_API int scape_create_ex(const scape_layout* layout, int W, double density,
   for (uint32_t i = 0; i < layout->n_tensors; i++) {
     if (layout->numel[i] > (1ull << 32)) return fail(nullptr, SCAPE_EINVAL, "tensor too large");
     N += layout->numel[i];
+    if (N >= (1ull << 32)) break;  // rejected below; stops the sum before it can wrap
   }
   if (N == 0 || N >= (1ull << 32))
     return fail(nullptr, SCAPE_EINVAL, "N=%llu must be in [1, 2^32)", (unsigned long long)N);

@@ -57,6 +57,9 @@ def _create(lib, numel, chunk, W, density, eps=1e-8):
     ([0], 1024, 2, 0.1, 1e-8, "N="),
     ([1 << 31, 1 << 31], 1024, 2, 0.1, 1e-8, "N="),
     ([1024], 1024, 2, 0.1, 0.0, "eps"),
+    ([1024], 1024, 2, float("nan"), 1e-8, "density"),
+    ([1024], 1024, 2, 0.1, float("nan"), "eps"),
+    ([1024], 1024, 2, 0.1, float("inf"), "hyper-parameters"),
 ])
 def test_create_rejects_bad_arguments(lib, numel, chunk, W, density, eps, what):
     rc, h = _create(lib, numel, chunk, W, density, eps)
@@ -69,6 +72,7 @@ def test_null_handles(lib):
     lib.scape_destroy(None)
     assert lib.scape_step(None, None, None) == scape.SCAPE_EINVAL
     assert lib.scape_mask(None, None) == scape.SCAPE_EINVAL
+    assert lib.scape_mask_async(None, None, None) == scape.SCAPE_EINVAL
     assert lib.scape_info(None, None) == scape.SCAPE_EINVAL
     assert lib.scape_read_sparse(None, 0, None, None, 0, 0, None) == scape.SCAPE_EINVAL
 

@@ -52,6 +52,10 @@ def test_flat_2p20_every_coordinate():
     (2048 + 7, 4, 512, 1.0),   # density 1: every coordinate, dense AdamS
     (65536 * 2 + 160, 2, 65536, 0.3),  # large k in a full chunk, 160-coordinate last chunk
     (70001, 64, 1024, 0.05),   # the largest W
+    (1, 1, 32, 1.0),           # one coordinate: one partial mask word, k = 1
+    (31, 2, 32, 0.5),          # N below one word, two workers on one chunk
+    (100, 7, 32, 0.25),        # 4 chunks, 7 workers: workers 4-6 own no chunk
+    (65536 * 2, 2, 65536, 1.0),  # k = 65536: every coordinate of full-size chunks
 ])
 def test_edge_shapes(N, W, chunk, density):
     wl = synth.tiny(N, W, chunk, density, seed=N)
