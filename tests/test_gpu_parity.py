@@ -339,6 +339,23 @@ def test_largest_n():
     _run_both(wl, 0.001, 2, chunk_ids=ids)
 
 
+def test_full_size_host_residuals_sampled():
+    # the whole-sector mapping at full size: 17.8 GB of residuals in host memory
+    wl = synth.WORKLOADS["llama-500m-w8"]
+    ids = sample_chunks(wl)
+    g = DeviceRun(wl, 0.01, flags=RESIDUAL_HOST)
+    r = OracleRun(wl, 0.01, chunk_ids=ids)
+    try:
+        assert g.sc.info["host_bytes"] >= wl.W * wl.N * 4
+        for t in range(3):
+            g.step()
+            r.step()
+            compare(g, r, f"step {t}")
+        check_full_mask(g)
+    finally:
+        g.close()
+
+
 def test_per_tensor_with_host_residuals_and_mask_stats():
     # both options at once, and the mask diagnostics on per-tensor chunks
     numel = [96, 20000 * 32, 64, 4096 + 33]
