@@ -50,28 +50,44 @@
 namespace scape {
 namespace {
 
-constexpr int kNT = 1024;
-constexpr int kNW = kNT / 32;
 constexpr uint32_t kCap = 2048;          // candidates ranked in shared memory
 constexpr uint32_t kRankCountMax = 1024; // up to this many: direct rank count
 constexpr int kTB = 47;                  // composite key bits
 
-// Dynamic shared memory layout (bytes), 188.8 KB.  L1 and shared memory share
-// one 256 KB array per SM and loads in flight are staged in L1: this layout
-// sits in the 196 KB carve-out (about 60 KB of L1 left).  Anything past
-// 196 KB moves the kernel to the 228 KB carve-out, where 28 KB of L1 cannot
-// hold enough loads in flight (measured: 24 KB more made the step 16% slower;
-// 24 KB less made no difference).
-constexpr uint32_t kOffKey16 = 0;                      // uint16[65536]
-constexpr uint32_t kOffHist = kOffKey16 + 65536 * 2;   // uint32[4096]
-constexpr uint32_t kOffWprev = kOffHist + 4096 * 4;    // uint32[2048]
-constexpr uint32_t kOffMword = kOffWprev + 2048 * 4;   // uint32[2048]
-constexpr uint32_t kOffWpre = kOffMword + 2048 * 4;    // uint16[2048]
-constexpr uint32_t kOffCand = kOffWpre + 2048 * 2;     // uint64[kCap]
-constexpr uint32_t kOffScan = kOffCand + kCap * 8;     // uint32[64]
-constexpr uint32_t kOffCtl = kOffScan + 64 * 4;        // uint32[32]
-constexpr uint32_t kOffStage = kOffCtl + 32 * 4;       // float[32 warps][32]
-constexpr uint32_t kSmemBytes = kOffStage + kNW * 32 * 4;
+// The CTA shape: NT threads, chunks of up to MAXC coordinates, MINB CTAs per
+// SM.  Dynamic shared memory layout (bytes) at the end.  L1 and shared memory
+// share one 256 KB array per SM and loads in flight are staged in L1: the
+// shapes below stay inside the 196 KB carve-out (about 60 KB of L1 left).
+// Anything past 196 KB moves the kernel to the 228 KB carve-out, where 28 KB
+// of L1 cannot hold enough loads in flight (measured: 24 KB more made the step
+// 16% slower; 24 KB less made no difference).
+template <int NT_, uint32_t MAXC_, int MINB_>
+struct Shape {
+  static constexpr int NT = NT_;
+  static constexpr int NW = NT / 32;
+  static constexpr uint32_t MAXC = MAXC_;
+  static constexpr uint32_t NWORDS = MAXC / 32;
+  static constexpr int MINB = MINB_;
+  static constexpr uint32_t OffKey16 = 0;                      // uint16[MAXC]
+  static constexpr uint32_t OffHist = OffKey16 + MAXC * 2;     // uint32[4096]
+  static constexpr uint32_t OffWprev = OffHist + 4096 * 4;     // uint32[NWORDS]
+  static constexpr uint32_t OffMword = OffWprev + NWORDS * 4;  // uint32[NWORDS]
+  static constexpr uint32_t OffWpre = OffMword + NWORDS * 4;   // uint16[NWORDS]
+  static constexpr uint32_t OffCand = OffWpre + NWORDS * 2;    // uint64[kCap]
+  static constexpr uint32_t OffScan = OffCand + kCap * 8;      // uint32[64]
+  static constexpr uint32_t OffCtl = OffScan + 64 * 4;         // uint32[32]
+  static constexpr uint32_t OffStage = OffCtl + 32 * 4;        // float[NW][32]
+  static constexpr uint32_t SmemBytes = OffStage + NW * 32 * 4;
+  static_assert(NWORDS <= 2 * NT, "phase 0 takes two mask words per thread");
+  static_assert(OffCand % 8 == 0, "candidate keys are 8-byte aligned");
+  static_assert(NW <= 32, "block scans keep one total per warp");
+  static_assert(MINB * (SmemBytes + 1024) <= 196 * 1024, "inside the 196 KB carve-out");
+};
+// Big: one 1024-thread CTA per SM, chunks up to 65536 (188.8 KB).  Small:
+// chunks up to 16384 leave most of a 1024-thread CTA idle and too few chunks
+// in flight, so two 512-thread CTAs share an SM (71.4 KB each).
+using Big = Shape<1024, kMaxChunk, 1>;
+using Small = Shape<512, 16384, 2>;
 
 // ctl[] slots
 enum { C_BIN = 0, C_ABOVE = 1, C_CNT = 2, C_NCAND = 3, C_SUB = 8 /* 16 entries */ };
@@ -88,17 +104,18 @@ struct Shared {
   float* stage;  // per warp: the tile's first 32 kept values, for one coalesced store
 };
 
+template <class K>
 __device__ __forceinline__ Shared carve(unsigned char* s) {
   Shared sh;
-  sh.key16 = reinterpret_cast<uint16_t*>(s + kOffKey16);
-  sh.hist = reinterpret_cast<uint32_t*>(s + kOffHist);
-  sh.wprev = reinterpret_cast<uint32_t*>(s + kOffWprev);
-  sh.mword = reinterpret_cast<uint32_t*>(s + kOffMword);
-  sh.wpre = reinterpret_cast<uint16_t*>(s + kOffWpre);
-  sh.cand = reinterpret_cast<unsigned long long*>(s + kOffCand);
-  sh.scan = reinterpret_cast<uint32_t*>(s + kOffScan);
-  sh.ctl = reinterpret_cast<uint32_t*>(s + kOffCtl);
-  sh.stage = reinterpret_cast<float*>(s + kOffStage);
+  sh.key16 = reinterpret_cast<uint16_t*>(s + K::OffKey16);
+  sh.hist = reinterpret_cast<uint32_t*>(s + K::OffHist);
+  sh.wprev = reinterpret_cast<uint32_t*>(s + K::OffWprev);
+  sh.mword = reinterpret_cast<uint32_t*>(s + K::OffMword);
+  sh.wpre = reinterpret_cast<uint16_t*>(s + K::OffWpre);
+  sh.cand = reinterpret_cast<unsigned long long*>(s + K::OffCand);
+  sh.scan = reinterpret_cast<uint32_t*>(s + K::OffScan);
+  sh.ctl = reinterpret_cast<uint32_t*>(s + K::OffCtl);
+  sh.stage = reinterpret_cast<float*>(s + K::OffStage);
   return sh;
 }
 
@@ -115,7 +132,7 @@ enum { PASS_OTHER = 0, PASS_OWNER = 1, PASS_BOOT = 2 };
 // PASS_OWNER also keeps the keys of |a| and their histogram; PASS_BOOT only
 // computes the step-0 accumulator a = e + (b1*u + c1*g) for its keys and
 // writes nothing to memory.
-template <int PASS>
+template <class K, int PASS>
 __device__ __forceinline__ void stream_worker(const FusedArgs& p, const Shared& sh,
                                               const Chunk& ch, int w) {
   constexpr bool KEYS = PASS != PASS_OTHER;
@@ -128,7 +145,7 @@ __device__ __forceinline__ void stream_worker(const FusedArgs& p, const Shared& 
   const float b1 = p.b1, c1 = p.c1;
   float* stage = sh.stage + warp * 32;
   const uint32_t ntile = (ch.L + 255) / 256;
-  for (uint32_t t = warp; t < ntile; t += kNW) {  // warp-uniform: every lane takes part
+  for (uint32_t t = warp; t < ntile; t += K::NW) {  // warp-uniform: every lane takes part
     const uint32_t i0 = t * 256 + lane * 8;
     const bool active = i0 < ch.L;
     uint32_t byte = 0, rank0 = 0, tile0 = 0;
@@ -230,7 +247,7 @@ __device__ __forceinline__ void stream_worker(const FusedArgs& p, const Shared& 
 // above) moves half the useful bytes per transfer; in HBM, L2 merges the
 // halves and the layout above, with twice the bytes in flight per thread, is
 // faster.
-template <int PASS>
+template <class K, int PASS>
 __device__ __forceinline__ void stream_worker_contig(const FusedArgs& p, const Shared& sh,
                                               const Chunk& ch, int w) {
   constexpr bool KEYS = PASS != PASS_OTHER;
@@ -244,7 +261,7 @@ __device__ __forceinline__ void stream_worker_contig(const FusedArgs& p, const S
   float* stage = sh.stage + warp * 32;
   const uint32_t ntile = (ch.L + 255) / 256;
   const uint32_t sft = (lane & 7) * 4;  // the group's nibble in its mask word
-  for (uint32_t t = warp; t < ntile; t += kNW) {  // warp-uniform: every lane takes part
+  for (uint32_t t = warp; t < ntile; t += K::NW) {  // warp-uniform: every lane takes part
     const uint32_t tile0 = WRITE ? (uint32_t)sh.wpre[t * 8] : 0u;  // first kept value's rank
     const uint32_t ia = t * 256 + lane * 4;  // group h starts at ia + 128 h
     uint32_t nr[2] = {0u, 0u};  // group h: mask nibble << 28 | rank of its first coordinate
@@ -360,6 +377,7 @@ __device__ __forceinline__ uint32_t owner_key(const FusedArgs& p, const Shared& 
 
 // Phase 2.  Leaves the chunk's mask words in sh.mword; returns false when the
 // chunk must be redone by the standalone select (too many tied candidates).
+template <class K>
 __device__ bool select_chunk(const FusedArgs& p, const Shared& sh, const Chunk& ch) {
   const int tid = threadIdx.x, lane = tid & 31;
   const uint32_t L = ch.L, k = ch.k;
@@ -369,7 +387,7 @@ __device__ bool select_chunk(const FusedArgs& p, const Shared& sh, const Chunk& 
   uint32_t r2 = 0, ncand = 0;
 
   if (k == 0 || k == L) {
-    for (uint32_t j = tid; j < ch.nw; j += kNT) {
+    for (uint32_t j = tid; j < ch.nw; j += K::NT) {
       uint32_t word = 0u;
       if (k != 0) word = (j == ch.nw - 1 && (L & 31)) ? ((1u << (L & 31)) - 1u) : 0xFFFFFFFFu;
       sh.mword[j] = word;
@@ -377,7 +395,7 @@ __device__ bool select_chunk(const FusedArgs& p, const Shared& sh, const Chunk& 
     __syncthreads();
     return true;
   }
-  find_bin<kNT>(sh.hist, 4096, k, sh.scan, sh.ctl);
+  find_bin<K::NT>(sh.hist, 4096, k, sh.scan, sh.ctl);
   const uint32_t b12 = sh.ctl[C_BIN], cnt12 = sh.ctl[C_CNT];
   const uint32_t r1 = k - sh.ctl[C_ABOVE];
   if (r1 == cnt12) {
@@ -387,7 +405,7 @@ __device__ bool select_chunk(const FusedArgs& p, const Shared& sh, const Chunk& 
     // 16 sub-buckets of the threshold bin
     if (tid < 16) sh.ctl[C_SUB + tid] = 0;
     __syncthreads();
-    for (uint32_t i = tid; i < L; i += kNT) {
+    for (uint32_t i = tid; i < L; i += K::NT) {
       const uint32_t k16 = sh.key16[i];
       if ((k16 >> 4) == b12) atomicAdd(&sh.ctl[C_SUB + (k16 & 15u)], 1u);
     }
@@ -415,7 +433,7 @@ __device__ bool select_chunk(const FusedArgs& p, const Shared& sh, const Chunk& 
       if (cnt16 > kCap) return false;  // uniform: every thread read the same cnt16
       ranked = true;
       // candidates: coordinates in bucket T16, with their full composite key
-      for (uint32_t base = (tid & ~31u); base < L; base += kNT) {
+      for (uint32_t base = (tid & ~31u); base < L; base += K::NT) {
         const uint32_t i = base + lane;
         const bool is = i < L && sh.key16[i] == T16;
         const unsigned bal = __ballot_sync(kFull, is);
@@ -438,7 +456,7 @@ __device__ bool select_chunk(const FusedArgs& p, const Shared& sh, const Chunk& 
   // 16-bit keys, no shared-memory bank conflicts) and lane r keeps the word
   const int warp = tid >> 5;
   const uint32_t tb = take_bucket ? T16 : T16 + 1;  // kept iff key16 >= tb
-  for (uint32_t j0 = (uint32_t)warp * 32; j0 < ch.nw; j0 += kNT) {
+  for (uint32_t j0 = (uint32_t)warp * 32; j0 < ch.nw; j0 += K::NT) {
     uint32_t mine = 0u;
     for (int r = 0; r < 32; r++) {
       const uint32_t i = (j0 + r) * 32 + lane;
@@ -453,7 +471,7 @@ __device__ bool select_chunk(const FusedArgs& p, const Shared& sh, const Chunk& 
   if (ranked) {
     if (ncand <= kRankCountMax) {
       // direct rank: keep candidate m iff fewer than r2 candidates are larger
-      for (uint32_t m = tid; m < ncand; m += kNT) {
+      for (uint32_t m = tid; m < ncand; m += K::NT) {
         const unsigned long long X = sh.cand[m];
         uint32_t above = 0;
         for (uint32_t o = 0; o < ncand; o++) above += sh.cand[o] > X;
@@ -471,15 +489,15 @@ __device__ bool select_chunk(const FusedArgs& p, const Shared& sh, const Chunk& 
         const int d = (kTB - pb) < 12 ? (kTB - pb) : 12;
         const int nb = 1 << d;
         const int shift = kTB - pb - d;
-        for (int i = tid; i < nb; i += kNT) sh.hist[i] = 0;
+        for (int i = tid; i < nb; i += K::NT) sh.hist[i] = 0;
         __syncthreads();
-        for (uint32_t m = tid; m < ncand; m += kNT) {
+        for (uint32_t m = tid; m < ncand; m += K::NT) {
           const unsigned long long X = sh.cand[m];
           if ((X >> (kTB - pb)) == pf)
             atomicAdd(&sh.hist[(uint32_t)(X >> shift) & (uint32_t)(nb - 1)], 1u);
         }
         __syncthreads();
-        find_bin<kNT>(sh.hist, nb, rr, sh.scan, sh.ctl);
+        find_bin<K::NT>(sh.hist, nb, rr, sh.scan, sh.ctl);
         const uint32_t b = sh.ctl[C_BIN], above = sh.ctl[C_ABOVE], cnt = sh.ctl[C_CNT];
         __syncthreads();
         rr -= above;
@@ -488,7 +506,7 @@ __device__ bool select_chunk(const FusedArgs& p, const Shared& sh, const Chunk& 
         if (rr == cnt) break;
       }
       const unsigned long long T = pf << (kTB - pb);
-      for (uint32_t m = tid; m < ncand; m += kNT) {
+      for (uint32_t m = tid; m < ncand; m += K::NT) {
         const unsigned long long X = sh.cand[m];
         if (X >= T) {
           const uint32_t i = 0xFFFFu - (uint32_t)(X & 0xFFFFu);
@@ -539,6 +557,7 @@ __device__ __forceinline__ void prefetch_worker_tile(const FusedArgs& p, uint64_
 // takes positions R0 + l, R0 + l + 32, ... (coalesced reads of the W rows, one
 // memory round trip per 32 kept coordinates) and hands each value to the lane
 // that holds the coordinate with a shuffle.
+template <class K>
 __device__ __forceinline__ void update_chunk(const FusedArgs& p, const Shared& sh,
                                              const Chunk& ch) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -546,7 +565,7 @@ __device__ __forceinline__ void update_chunk(const FusedArgs& p, const Shared& s
   float* __restrict__ vv = p.v + ch.c0;
   const float b2 = p.b2, c2 = p.c2, lr = p.lr, wd = p.wd, eps = p.eps, invW = p.invW;
   const uint32_t ntile = (ch.L + 255) / 256;
-  for (uint32_t t = warp; t < ntile; t += kNW) {  // warp-uniform: every lane takes part
+  for (uint32_t t = warp; t < ntile; t += K::NW) {  // warp-uniform: every lane takes part
     const uint32_t i0 = t * 256 + lane * 8;
     const bool active = i0 < ch.L;
     uint32_t byte = 0, local0 = 0;
@@ -627,18 +646,18 @@ __device__ __forceinline__ void update_chunk(const FusedArgs& p, const Shared& s
   }
 }
 
-template <int PASS, bool CONTIG>
+template <class K, int PASS, bool CONTIG>
 __device__ __forceinline__ void stream_pass(const FusedArgs& p, const Shared& sh, const Chunk& ch,
                                             int w) {
-  if (CONTIG) stream_worker_contig<PASS>(p, sh, ch, w);
-  else stream_worker<PASS>(p, sh, ch, w);
+  if (CONTIG) stream_worker_contig<K, PASS>(p, sh, ch, w);
+  else stream_worker<K, PASS>(p, sh, ch, w);
 }
 
 // CONTIG: residual rows in mapped host memory (whole-sector access mapping)
-template <bool CONTIG>
-__global__ __launch_bounds__(kNT, 1) void step_chunks(const FusedArgs p) {
+template <class K, bool CONTIG>
+__global__ __launch_bounds__(K::NT, K::MINB) void step_chunks(const FusedArgs p) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  const Shared sh = carve(smem_raw);
+  const Shared sh = carve<K>(smem_raw);
   const int tid = threadIdx.x;
 
   for (uint64_t c = blockIdx.x; c < p.n_ch; c += gridDim.x) {
@@ -658,7 +677,7 @@ __global__ __launch_bounds__(kNT, 1) void step_chunks(const FusedArgs p) {
     }
     ch.nw = (ch.L + 31) / 32;
     ch.owner = (int)(c / p.q);
-    if (!SCAPE_CHECK(p.dbg, ch.c0 + ch.L <= p.N && ch.L <= kMaxChunk, CHK_CHUNK, ch.c0)) continue;
+    if (!SCAPE_CHECK(p.dbg, ch.c0 + ch.L <= p.N && ch.L <= K::MAXC, CHK_CHUNK, ch.c0)) continue;
 
     // phase 0: M_{t-1} words of the chunk, their popcount prefix; clear the histogram
     {
@@ -671,26 +690,26 @@ __global__ __launch_bounds__(kNT, 1) void step_chunks(const FusedArgs p) {
       }
       const uint32_t cnt = __popc(w0) + __popc(w1);
       uint32_t total;
-      const uint32_t inc = block_incl_scan<kNT>(cnt, sh.scan, &total);
-      if (j0 < 2048) {
+      const uint32_t inc = block_incl_scan<K::NT>(cnt, sh.scan, &total);
+      if (j0 < K::NWORDS) {
         sh.wprev[j0] = w0;
         sh.wprev[j0 + 1] = w1;
         sh.wpre[j0] = (uint16_t)(inc - cnt);
         sh.wpre[j0 + 1] = (uint16_t)(inc - cnt + __popc(w0));
       }
-      for (int i = tid; i < 4096; i += kNT) sh.hist[i] = 0;
+      for (int i = tid; i < 4096; i += K::NT) sh.hist[i] = 0;
       __syncthreads();
     }
 
     if (p.boot) {
       // step 0, first launch: M_{-1} of this chunk from the owner's step-0
       // accumulator (read only), ranked on chip like M_t below
-      stream_pass<PASS_BOOT, CONTIG>(p, sh, ch, ch.owner);
+      stream_pass<K, PASS_BOOT, CONTIG>(p, sh, ch, ch.owner);
       __syncthreads();
-      const bool ok = select_chunk(p, sh, ch);
+      const bool ok = select_chunk<K>(p, sh, ch);
       if (ok) {
         uint32_t* mo = p.mout + ch.c0 / 32;
-        for (uint32_t j = tid; j < ch.nw; j += kNT) mo[j] = sh.mword[j];
+        for (uint32_t j = tid; j < ch.nw; j += K::NT) mo[j] = sh.mword[j];
       } else if (tid == 0) {
         p.fallback[c] = 1u;
         atomicAdd(p.n_fallback, 1u);
@@ -701,15 +720,15 @@ __global__ __launch_bounds__(kNT, 1) void step_chunks(const FusedArgs p) {
     }
 
     // phase 1: the owner's pass, keeping its keys
-    stream_pass<PASS_OWNER, CONTIG>(p, sh, ch, ch.owner);
+    stream_pass<K, PASS_OWNER, CONTIG>(p, sh, ch, ch.owner);
     if (p.W > 1) prefetch_worker_tile(p, ch.c0, ch.L, ch.owner == 0 ? 1 : 0);
     __syncthreads();
 
     // phase 2: top-k of the owner's |a| -> mask words of M_t
-    const bool ok = select_chunk(p, sh, ch);
+    const bool ok = select_chunk<K>(p, sh, ch);
     if (ok) {
       uint32_t* mo = p.mout + ch.c0 / 32;
-      for (uint32_t j = tid; j < ch.nw; j += kNT) mo[j] = sh.mword[j];
+      for (uint32_t j = tid; j < ch.nw; j += K::NT) mo[j] = sh.mword[j];
     } else if (tid == 0) {
       p.fallback[c] = 1u;
       atomicAdd(p.n_fallback, 1u);
@@ -718,7 +737,7 @@ __global__ __launch_bounds__(kNT, 1) void step_chunks(const FusedArgs p) {
 
     // phase 3: every other worker
     for (int w = 0; w < p.W; w++)
-      if (w != ch.owner) stream_pass<PASS_OTHER, CONTIG>(p, sh, ch, w);
+      if (w != ch.owner) stream_pass<K, PASS_OTHER, CONTIG>(p, sh, ch, w);
     {
       const uint32_t i0 = (tid >> 5) * 256 + (tid & 31) * 8;
       if (i0 + 8 <= ch.L) {
@@ -729,7 +748,7 @@ __global__ __launch_bounds__(kNT, 1) void step_chunks(const FusedArgs p) {
     __syncthreads();
 
     // phase 4: synchronized buffer, second moment, parameters
-    update_chunk(p, sh, ch);
+    update_chunk<K>(p, sh, ch);
     {
       const uint64_t cn = c + gridDim.x;
       if (cn < p.n_ch && !p.chunks && !p.boot) {
@@ -745,27 +764,37 @@ __global__ __launch_bounds__(kNT, 1) void step_chunks(const FusedArgs p) {
 
 }  // namespace
 
-cudaError_t launch_step_chunks(const FusedArgs& a, cudaStream_t s) {
-  // the shared-memory opt-in is per device and per instantiation
-  static std::atomic<uint64_t> configured[2];
-  const int contig = a.e_host ? 1 : 0;
+namespace {
+
+// The shared-memory opt-in is per device and per instantiation.
+template <class K, bool CONTIG>
+cudaError_t launch_shape(const FusedArgs& a, cudaStream_t s) {
+  static std::atomic<uint64_t> configured{0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   const uint64_t bit = dev < 64 ? (1ull << dev) : 0ull;  // devices past 64: set every launch
-  if (!(configured[contig].load() & bit)) {
-    e = cudaFuncSetAttribute(contig ? step_chunks<true> : step_chunks<false>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  if (!(configured.load() & bit)) {
+    e = cudaFuncSetAttribute(step_chunks<K, CONTIG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)K::SmemBytes);
     if (e != cudaSuccess) return e;
-    configured[contig].fetch_or(bit);
+    configured.fetch_or(bit);
   }
-  uint64_t grid = (uint64_t)num_sms();
+  uint64_t grid = (uint64_t)num_sms() * K::MINB;
   if (grid > a.n_ch) grid = a.n_ch;
-  if (contig)
-    step_chunks<true><<<(unsigned)grid, kNT, kSmemBytes, s>>>(a);
-  else
-    step_chunks<false><<<(unsigned)grid, kNT, kSmemBytes, s>>>(a);
+  step_chunks<K, CONTIG><<<(unsigned)grid, K::NT, K::SmemBytes, s>>>(a);
   return cudaGetLastError();
+}
+
+}  // namespace
+
+// Chunks of up to 16384 coordinates take the two-CTAs-per-SM shape; every
+// chunk of the handle is at most C long (per-tensor chunks too).
+cudaError_t launch_step_chunks(const FusedArgs& a, cudaStream_t s) {
+  const bool small = a.C <= Small::MAXC;
+  if (a.e_host)
+    return small ? launch_shape<Small, true>(a, s) : launch_shape<Big, true>(a, s);
+  return small ? launch_shape<Small, false>(a, s) : launch_shape<Big, false>(a, s);
 }
 
 }  // namespace scape

@@ -108,7 +108,7 @@ __device__ __forceinline__ float bf16lo(uint32_t x) { return __uint_as_float(x <
 __device__ __forceinline__ float bf16hi(uint32_t x) { return __uint_as_float(x & 0xFFFF0000u); }
 __device__ __forceinline__ float bf16f(uint16_t h) { return __uint_as_float((uint32_t)h << 16); }
 
-// Streaming 16-byte load that is not kept in L1 (read-once data).
+// Streaming 8- and 16-byte loads that are not kept in L1 (read-once data).
 __device__ __forceinline__ uint2 ld_stream_u2(const void* p) {
   uint2 r;
   asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
