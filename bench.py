@@ -412,7 +412,17 @@ def run_scape(args, wl, density):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        n_ch, n_st = (128, 14) if N > 1 << 24 else (16, 8)
+        # sized from a short calibration run to about 12 s of oracle time:
+        # 14 steps over as many whole chunks as that allows, or, when every
+        # chunk fits, every chunk over as many steps
+        nch = -(-N // wl.chunk)
+        r0, _, _, _ = oracle_sample(wl, density, min(8, nch), 3)
+        work = r0 * 12.0  # coordinate-steps
+        n_st = 14
+        n_ch = int(work / (n_st * wl.chunk))
+        if n_ch >= nch:
+            n_ch, n_st = nch, max(14, int(work / N))
+        n_ch = max(1, n_ch)
         rate, dt, n, nc = oracle_sample(wl, density, n_ch, n_st)
         cpu = {"value": rate, "unit": "params/s", "cores": 1, "kind": "oracle",
                "sample": f"{nc} whole chunks ({n} params) of {wl.name}, W={W}, density {density}, "
