@@ -51,6 +51,8 @@ def parse():
     ap.add_argument("--mask-stats", action="store_true",
                     help="report mask overlap and the fill-in of per-worker global top-k")
     ap.add_argument("--workers", type=int, default=None, help="override W of the workload")
+    ap.add_argument("--seed", type=int, default=None,
+                    help="override the workload's generator seed (recorded in config)")
     ap.add_argument("--per-tensor", action="store_true", help="chunks restart at every tensor")
     ap.add_argument("--residual-host", action="store_true",
                     help="keep the residuals in page-locked host memory")
@@ -214,7 +216,7 @@ def run_reference(args, wl, density):
         "ms_per_step": per_step_ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": wl.name, "N": wl.N, "W": wl.W, "density": density,
-                   "chunk": wl.chunk, "sample_params": n},
+                   "chunk": wl.chunk, "seed": wl.seed, "sample_params": n},
         "cpu_baseline": {"value": rate, "unit": "params/s", "cores": 1, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": rate, "unit": "params/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -462,6 +464,7 @@ def run_scape(args, wl, density):
         "dtype": "f32",
         "data": "synthetic",
         "config": {"workload": wl.name, "N": N, "W": W, "density": density, "chunk": wl.chunk,
+                   "seed": wl.seed,
                    "K": K, "grad_dtype": "bf16", "grad_batches": n_batches,
                    "chunking": "per-tensor" if args.per_tensor else "flat",
                    "residuals": "host (page-locked)" if args.residual_host else "HBM",
@@ -498,9 +501,11 @@ def main():
     if args.impl == "scape" and args.warmup < 1:
         raise SystemExit("--warmup must be >= 1 (the first warm-up step is step 0)")
     wl = synth.WORKLOADS[args.workload]
+    import dataclasses
     if args.workers is not None:
-        import dataclasses
         wl = dataclasses.replace(wl, W=args.workers)
+    if args.seed is not None:
+        wl = dataclasses.replace(wl, seed=args.seed)
     density = args.density if args.density is not None else wl.densities[0]
     if args.impl == "reference":
         run_reference(args, wl, density)
