@@ -56,16 +56,20 @@ def test_flat_2p20_every_coordinate():
     (31, 2, 32, 0.5),          # N below one word, two workers on one chunk
     (100, 7, 32, 0.25),        # 4 chunks, 7 workers: workers 4-6 own no chunk
     (65536 * 2, 2, 65536, 1.0),  # k = 65536: every coordinate of full-size chunks
+    (16384 * 3 + 100, 3, 16384, 0.3),  # the largest chunk of the 512-thread shape
+    (16416 * 2 + 50, 2, 16416, 0.05),  # the smallest chunk of the 1024-thread shape
 ])
 def test_edge_shapes(N, W, chunk, density):
     wl = synth.tiny(N, W, chunk, density, seed=N)
     _run_both(wl, density, 4)
 
 
-def test_heavy_ties_overflow_candidates():
+@pytest.mark.parametrize("chunk", [65536, 16384])
+def test_heavy_ties_overflow_candidates(chunk):
     # Student-t means on a 2^-14 grid: |a| takes few hundred values, so the bin
-    # holding the threshold exceeds the shared-memory candidate list.
-    wl = synth.tiny(65536 * 3, 3, 65536, 0.1, kind=synth.SYN_STUDENT_Q, seed=3)
+    # holding the threshold exceeds the shared-memory candidate list (both
+    # CTA shapes of the step kernel)
+    wl = synth.tiny(chunk * 3, 3, chunk, 0.1, kind=synth.SYN_STUDENT_Q, seed=3)
     _run_both(wl, 0.1, 4)
 
 
@@ -115,23 +119,26 @@ def test_loaded_residuals_select_exactly():
         g.close()
 
 
+@pytest.mark.parametrize("chunk,density", [(65536, 0.01), (16384, 0.04)])
 @pytest.mark.parametrize("n_high,n_tied,expect_fallback",
                          [(300, 400, False), (100, 1500, False), (100, 3000, True)])
-def test_tied_bucket_paths(n_high, n_tied, expect_fallback):
-    # One 65536 chunk per worker, k = 655: n_high keys of 2.0 and n_tied keys
-    # of 1.0 (the rest 0.5); n_high < 655 < n_high + n_tied puts the threshold
-    # inside the 16-bit bucket of 1.0, which then holds n_tied tied keys.
-    # 400 -> ranked directly, 1500 -> radix among the on-chip candidates,
-    # 3000 -> more than the on-chip list holds, redone by the standalone select.
-    wl = synth.tiny(65536 * 2, 2, 65536, 0.01, beta1=0.0)
+def test_tied_bucket_paths(chunk, density, n_high, n_tied, expect_fallback):
+    # Two chunks per worker with k = 655 (both CTA shapes of the step kernel):
+    # n_high keys of 2.0 and n_tied keys of 1.0 (the rest 0.5); n_high < 655 <
+    # n_high + n_tied puts the threshold inside the 16-bit bucket of 1.0, which
+    # then holds n_tied tied keys.  400 -> ranked directly, 1500 -> radix among
+    # the on-chip candidates, 3000 -> more than the on-chip list holds, redone
+    # by the standalone select.
+    wl = synth.tiny(chunk * 2, 2, chunk, density, beta1=0.0)
+    assert int(np.floor(density * chunk)) == 655
     rng = np.random.default_rng(n_tied)
     e0 = np.full((2, wl.N), 0.5, np.float32)
     for w in range(2):
         for c in range(2):
-            pos = c * 65536 + rng.permutation(65536)[: n_high + n_tied]
+            pos = c * chunk + rng.permutation(chunk)[: n_high + n_tied]
             e0[w, pos[:n_high]] = 2.0
             e0[w, pos[n_high:]] = -1.0
-    g, r = DeviceRun(wl, 0.01), OracleRun(wl, 0.01)
+    g, r = DeviceRun(wl, density), OracleRun(wl, density)
     try:
         for w in range(2):
             g.sc.load(E, e0[w], w)
