@@ -34,6 +34,9 @@
  *   - "stream" is a cudaStream_t passed as void* (NULL = legacy default
  *     stream).  scape_step* only enqueue work on it and return; readers
  *     (scape_mask, scape_read_*) first wait for the last step's stream.
+ *     Consecutive steps of one handle must run in order: on one stream, or
+ *     on streams the caller orders (each step reads what the previous one
+ *     wrote; the library adds no wait between them).
  *   - Pointers documented as "host or device" may be either (copies use
  *     cudaMemcpyDefault under unified addressing).
  *   - A handle is not thread-safe; separate handles are independent.

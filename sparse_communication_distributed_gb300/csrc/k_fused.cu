@@ -659,6 +659,7 @@ __global__ __launch_bounds__(K::NT, K::MINB) void step_chunks(const FusedArgs p)
   extern __shared__ __align__(16) unsigned char smem_raw[];
   const Shared sh = carve<K>(smem_raw);
   const int tid = threadIdx.x;
+  if (p.pending_clear && blockIdx.x == 0 && tid == 0) *p.pending_clear = 0u;
 
   for (uint64_t c = blockIdx.x; c < p.n_ch; c += gridDim.x) {
     Chunk ch;

@@ -52,7 +52,8 @@ struct scape_handle {
   uint32_t* fallback = nullptr;    // per chunk, see k_fused.cu
   uint32_t* n_fallback = nullptr;  // chunks redone by the standalone select (running total)
   uint32_t* dbg = nullptr;         // check-failure record of debug builds (4 words)
-  uint32_t* pending = nullptr;     // chunks flagged by the current step-kernel launch
+  uint32_t* pending = nullptr;     // two counters of flagged chunks, used in turn by the
+  uint32_t launches = 0;           // step-kernel launches (launch i counts into slot i % 2)
   uint16_t* stage = nullptr;  // scape_step_host staging, W x N bf16
   uint32_t* diag = nullptr;   // scape_mask_stats: two masks + 3 counters (first use)
   uint32_t flags = 0;         // SCAPE_CHUNK_PER_TENSOR | SCAPE_RESIDUAL_HOST
@@ -326,7 +327,7 @@ SCAPE_API int scape_create_ex(const scape_layout* layout, int W, double density,
   if (e == cudaSuccess) e = dalloc(h, &h->fallback, h->n_ch);
   if (e == cudaSuccess) e = dalloc(h, &h->n_fallback, 1);
   if (e == cudaSuccess) e = dalloc(h, &h->dbg, 4);
-  if (e == cudaSuccess) e = dalloc(h, &h->pending, 1);
+  if (e == cudaSuccess) e = dalloc(h, &h->pending, 2);
   if (e == cudaSuccess && (flags & SCAPE_CHUNK_PER_TENSOR)) {
     e = dalloc(h, &h->chunks_dev, h->n_ch);
     if (e == cudaSuccess)
@@ -414,7 +415,6 @@ static void fill_fused(const scape_handle* h, const uint16_t* const* g, const ui
   a.mout = mout;
   a.fallback = h->fallback;
   a.n_fallback = h->n_fallback;
-  a.pending = h->pending;
   a.chunks = h->chunks_dev;
   a.dbg = h->dbg;
   a.N = h->N;
@@ -436,6 +436,17 @@ static void fill_fused(const scape_handle* h, const uint16_t* const* g, const ui
   a.wd = h->wd;
   a.eps = h->eps;
   a.invW = h->invW;
+}
+
+// Launch i of the step kernel counts the chunks it flags into pending[i % 2]
+// and zeroes the other slot for launch i + 1; the select after launch i-1,
+// the only reader of that slot, has finished by then (same stream).  No
+// per-step memset is needed.
+static void take_pending_slot(scape_handle* h, FusedArgs& a, SelectArgs& sa) {
+  const uint32_t i = h->launches++ & 1u;
+  a.pending = h->pending + i;
+  a.pending_clear = h->pending + (1u - i);
+  sa.pending = h->pending + i;
 }
 
 static int step_device(scape_handle* h, const uint16_t* const* g, cudaStream_t s) {
@@ -478,29 +489,25 @@ static int step_device(scape_handle* h, const uint16_t* const* g, cudaStream_t s
     fill_fused(h, g, mprev, mprev, a);
     a.mprev = nullptr;
     a.boot = 1;
-    if ((e = cudaMemsetAsync(h->pending, 0, sizeof(uint32_t), s)) != cudaSuccess ||
-        (e = launch_step_chunks(a, s)) != cudaSuccess)
-      return cuda_fail(h, e, "step-0 mask");
+    take_pending_slot(h, a, sa);
+    if ((e = launch_step_chunks(a, s)) != cudaSuccess) return cuda_fail(h, e, "step-0 mask");
     sa.mprev = nullptr;  // chunks with too many tied keys: the standalone select
     sa.mout = mprev;
     sa.flags = h->fallback;
-    sa.pending = h->pending;
     if ((e = launch_select(sa, true, s)) != cudaSuccess) return cuda_fail(h, e, "select (step 0)");
     pt.done();
   }
   {
     fill_fused(h, g, mprev, mcur, a);
+    take_pending_slot(h, a, sa);
     PhaseTimer pt(h, SCAPE_PH_STEP, s);
-    if ((e = cudaMemsetAsync(h->pending, 0, sizeof(uint32_t), s)) != cudaSuccess ||
-        (e = launch_step_chunks(a, s)) != cudaSuccess)
-      return cuda_fail(h, e, "step kernel");
+    if ((e = launch_step_chunks(a, s)) != cudaSuccess) return cuda_fail(h, e, "step kernel");
     pt.done();
   }
   {  // chunks whose threshold bucket overflowed the on-chip candidate list
     sa.mprev = mprev;
     sa.mout = mcur;
     sa.flags = h->fallback;
-    sa.pending = h->pending;
     PhaseTimer pt(h, SCAPE_PH_SELECT_FALLBACK, s);
     if ((e = launch_select(sa, false, s)) != cudaSuccess) return cuda_fail(h, e, "select (fallback)");
     pt.done();

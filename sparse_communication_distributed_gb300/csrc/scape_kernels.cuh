@@ -41,7 +41,8 @@ struct FusedArgs {
   uint32_t* mout;
   uint32_t* fallback;    // per chunk: 1 = selection left to the standalone select
   uint32_t* n_fallback;  // count of such chunks (diagnostic)
-  uint32_t* pending;     // chunks flagged by this launch (zeroed before it; may be NULL)
+  uint32_t* pending;     // chunks flagged by this launch (zero at its start; may be NULL)
+  uint32_t* pending_clear;  // zeroed by the launch (the next launch's counter); may be NULL
   const ChunkDesc* chunks;  // NULL: chunk c = [c*C, c*C + C) of the flat vector
   uint64_t N, Np, Kp, n_ch, q;
   uint32_t C, k_full, k_last;
