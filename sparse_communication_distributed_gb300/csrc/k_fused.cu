@@ -659,6 +659,8 @@ __global__ __launch_bounds__(K::NT, K::MINB) void step_chunks(const FusedArgs p)
   extern __shared__ __align__(16) unsigned char smem_raw[];
   const Shared sh = carve<K>(smem_raw);
   const int tid = threadIdx.x;
+  grid_dependency_wait();    // the previous step's select has finished
+  grid_launch_dependents();  // every CTA is resident: the select may launch
   if (p.pending_clear && blockIdx.x == 0 && tid == 0) *p.pending_clear = 0u;
 
   for (uint64_t c = blockIdx.x; c < p.n_ch; c += gridDim.x) {
@@ -783,8 +785,18 @@ cudaError_t launch_shape(const FusedArgs& a, cudaStream_t s) {
   }
   uint64_t grid = (uint64_t)num_sms() * K::MINB;
   if (grid > a.n_ch) grid = a.n_ch;
-  step_chunks<K, CONTIG><<<(unsigned)grid, K::NT, K::SmemBytes, s>>>(a);
-  return cudaGetLastError();
+  // launched while the grid ahead of it drains (it waits for it on the GPU)
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(K::NT);
+  cfg.dynamicSmemBytes = K::SmemBytes;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, step_chunks<K, CONTIG>, a);
 }
 
 }  // namespace

@@ -276,6 +276,8 @@ __device__ void select_one(const SelectArgs& p, SelectSmem& sm, const uint64_t c
 template <int SRC>
 __global__ __launch_bounds__(kNT, 2) void select_topk(const SelectArgs p) {
   __shared__ SelectSmem sm;
+  grid_dependency_wait();    // the step kernel has finished
+  grid_launch_dependents();  // every CTA is resident: the next step may launch
   if (p.pending && *p.pending == 0u) return;  // the step kernel flagged no chunk
   for (uint64_t c = blockIdx.x; c < p.n_ch; c += gridDim.x) {
     if (p.flags && p.flags[c] == 0u) continue;
@@ -290,11 +292,18 @@ __global__ __launch_bounds__(kNT, 2) void select_topk(const SelectArgs p) {
 cudaError_t launch_select(const SelectArgs& a, bool boot, cudaStream_t s) {
   uint64_t grid = (uint64_t)num_sms() * 2;
   if (grid > a.n_ch) grid = a.n_ch;
-  if (boot)
-    select_topk<SRC_BOOT><<<(unsigned)grid, kNT, 0, s>>>(a);
-  else
-    select_topk<SRC_STATE><<<(unsigned)grid, kNT, 0, s>>>(a);
-  return cudaGetLastError();
+  // launched while the step kernel drains (it waits for it on the GPU)
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kNT);
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return boot ? cudaLaunchKernelEx(&cfg, select_topk<SRC_BOOT>, a)
+              : cudaLaunchKernelEx(&cfg, select_topk<SRC_STATE>, a);
 }
 
 }  // namespace scape

@@ -108,6 +108,19 @@ __device__ __forceinline__ float bf16lo(uint32_t x) { return __uint_as_float(x <
 __device__ __forceinline__ float bf16hi(uint32_t x) { return __uint_as_float(x & 0xFFFF0000u); }
 __device__ __forceinline__ float bf16f(uint16_t h) { return __uint_as_float((uint32_t)h << 16); }
 
+// Programmatic dependent launch.  A grid launched with the programmatic
+// stream serialization attribute may start before the grid ahead of it on the
+// stream has finished; grid_dependency_wait() returns once that grid has
+// completed and its memory is visible (at once for a plain launch), and no
+// thread touches global memory before it.  grid_launch_dependents() lets the
+// next such grid launch; it then waits in its own grid_dependency_wait().
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Streaming 8- and 16-byte loads that are not kept in L1 (read-once data).
 __device__ __forceinline__ uint2 ld_stream_u2(const void* p) {
   uint2 r;
