@@ -414,12 +414,13 @@ def run_scape(args, wl, density):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        # sized from a short calibration run to about 12 s of oracle time:
+        # sized from a short calibration run (which includes step 0, so it
+        # reads slow) to about 12 s of oracle time:
         # 14 steps over as many whole chunks as that allows, or, when every
         # chunk fits, every chunk over as many steps
         nch = -(-N // wl.chunk)
         r0, _, _, _ = oracle_sample(wl, density, min(8, nch), 3)
-        work = r0 * 12.0  # coordinate-steps
+        work = r0 * 15.0  # coordinate-steps
         n_st = 14
         n_ch = int(work / (n_st * wl.chunk))
         if n_ch >= nch:
