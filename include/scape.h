@@ -36,7 +36,10 @@
  *     (scape_mask, scape_read_*) first wait for the last step's stream.
  *     Consecutive steps of one handle must run in order: on one stream, or
  *     on streams the caller orders (each step reads what the previous one
- *     wrote; the library adds no wait between them).
+ *     wrote; the library adds no wait between them).  A step is not meant to
+ *     be captured into a CUDA graph and replayed: the handle's host-side
+ *     state (which mask buffer is M_{t-1}, the step count) advances once per
+ *     call, not per replay.
  *   - Pointers documented as "host or device" may be either (copies use
  *     cudaMemcpyDefault under unified addressing).
  *   - A handle is not thread-safe; separate handles are independent.
