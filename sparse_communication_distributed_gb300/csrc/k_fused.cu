@@ -785,6 +785,10 @@ cudaError_t launch_shape(const FusedArgs& a, cudaStream_t s) {
   }
   uint64_t grid = (uint64_t)num_sms() * K::MINB;
   if (grid > a.n_ch) grid = a.n_ch;
+  {  // the same number of rounds with the last one as full as it gets
+    const uint64_t rounds = (a.n_ch + grid - 1) / grid;
+    grid = (a.n_ch + rounds - 1) / rounds;
+  }
   // launched while the grid ahead of it drains (it waits for it on the GPU)
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
