@@ -405,7 +405,17 @@ __device__ bool select_chunk(const FusedArgs& p, const Shared& sh, const Chunk& 
     // 16 sub-buckets of the threshold bin
     if (tid < 16) sh.ctl[C_SUB + tid] = 0;
     __syncthreads();
-    for (uint32_t i = tid; i < L; i += K::NT) {
+    const uint32_t L8 = L & ~7u;  // 8 keys per 16-byte load, then the ragged end
+    for (uint32_t i = tid * 8; i < L8; i += K::NT * 8) {
+      const uint4 v = *reinterpret_cast<const uint4*>(sh.key16 + i);
+      const uint32_t kw[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int q = 0; q < 8; q++) {
+        const uint32_t k16 = (kw[q >> 1] >> (16 * (q & 1))) & 0xFFFFu;
+        if ((k16 >> 4) == b12) atomicAdd(&sh.ctl[C_SUB + (k16 & 15u)], 1u);
+      }
+    }
+    for (uint32_t i = L8 + tid; i < L; i += K::NT) {
       const uint32_t k16 = sh.key16[i];
       if ((k16 >> 4) == b12) atomicAdd(&sh.ctl[C_SUB + (k16 & 15u)], 1u);
     }
@@ -432,18 +442,34 @@ __device__ bool select_chunk(const FusedArgs& p, const Shared& sh, const Chunk& 
     if (!take_bucket) {
       if (cnt16 > kCap) return false;  // uniform: every thread read the same cnt16
       ranked = true;
-      // candidates: coordinates in bucket T16, with their full composite key
-      for (uint32_t base = (tid & ~31u); base < L; base += K::NT) {
-        const uint32_t i = base + lane;
-        const bool is = i < L && sh.key16[i] == T16;
-        const unsigned bal = __ballot_sync(kFull, is);
+      // candidates: coordinates in bucket T16, with their full composite key.
+      // Lane l of a warp tests keys [b0 + 8 l, b0 + 8 l + 8) (one 16-byte
+      // load); the rare rounds with a match allocate slots by a warp scan.
+      for (uint32_t b0 = (tid & ~31u) * 8; b0 < L; b0 += K::NT * 8) {
+        const uint32_t i0 = b0 + lane * 8;
+        uint32_t m8 = 0;  // bit j: coordinate i0 + j is in the bucket
+        if (i0 + 8 <= L) {
+          const uint4 v = *reinterpret_cast<const uint4*>(sh.key16 + i0);
+          const uint32_t kw[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int q = 0; q < 8; q++)
+            m8 |= (uint32_t)(((kw[q >> 1] >> (16 * (q & 1))) & 0xFFFFu) == T16) << q;
+        } else {
+          for (uint32_t q = 0; i0 + q < L; q++) m8 |= (uint32_t)(sh.key16[i0 + q] == T16) << q;
+        }
+        if (!__any_sync(kFull, m8 != 0u)) continue;  // warp-uniform
+        const uint32_t n = __popc(m8);
+        const uint32_t incl = warp_incl_scan(n, lane);
         uint32_t pos = 0;
-        if (lane == 0 && bal) pos = atomicAdd(&sh.ctl[C_NCAND], __popc(bal));
-        pos = __shfl_sync(kFull, pos, 0);
-        const uint32_t slot = pos + __popc(bal & ((1u << lane) - 1u));
-        if (is && SCAPE_CHECK(p.dbg, slot < kCap, CHK_CAND, ch.c0 + i)) {
-          const uint32_t key = owner_key(p, sh, ch, i);
-          sh.cand[slot] = ((unsigned long long)key << 16) | (unsigned long long)(0xFFFFu - i);
+        if (lane == 31) pos = atomicAdd(&sh.ctl[C_NCAND], incl);
+        pos = __shfl_sync(kFull, pos, 31) + incl - n;
+        for (uint32_t mm = m8; mm; mm &= mm - 1u) {
+          const uint32_t i = i0 + (uint32_t)(__ffs(mm) - 1);
+          const uint32_t slot = pos++;
+          if (SCAPE_CHECK(p.dbg, slot < kCap, CHK_CAND, ch.c0 + i)) {
+            const uint32_t key = owner_key(p, sh, ch, i);
+            sh.cand[slot] = ((unsigned long long)key << 16) | (unsigned long long)(0xFFFFu - i);
+          }
         }
       }
       __syncthreads();
@@ -451,20 +477,27 @@ __device__ bool select_chunk(const FusedArgs& p, const Shared& sh, const Chunk& 
     }
   }
 
-  // mask words from the stored keys: each warp builds 32 words by ballot, in
-  // round r its lanes test the 32 coordinates of word j0 + r (consecutive
-  // 16-bit keys, no shared-memory bank conflicts) and lane r keeps the word
+  // mask words from the stored keys: lane l of a warp tests keys
+  // [b0 + 8 l, b0 + 8 l + 8) (one 16-byte load; a warp covers 8 words) into
+  // a byte, and the 4 lanes of a word merge their bytes by two xor-shuffles
   const int warp = tid >> 5;
   const uint32_t tb = take_bucket ? T16 : T16 + 1;  // kept iff key16 >= tb
-  for (uint32_t j0 = (uint32_t)warp * 32; j0 < ch.nw; j0 += K::NT) {
-    uint32_t mine = 0u;
-    for (int r = 0; r < 32; r++) {
-      const uint32_t i = (j0 + r) * 32 + lane;
-      const bool set = i < L && sh.key16[i] >= tb;
-      const unsigned b = __ballot_sync(kFull, set);
-      if (lane == r) mine = b;
+  for (uint32_t b0 = (uint32_t)warp * 256; b0 < ch.nw * 32; b0 += K::NT * 8) {
+    const uint32_t i0 = b0 + lane * 8;
+    uint32_t byte = 0u;
+    if (i0 + 8 <= L) {
+      const uint4 v = *reinterpret_cast<const uint4*>(sh.key16 + i0);
+      const uint32_t kw[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int q = 0; q < 8; q++)
+        byte |= (uint32_t)(((kw[q >> 1] >> (16 * (q & 1))) & 0xFFFFu) >= tb) << q;
+    } else {
+      for (uint32_t q = 0; i0 + q < L; q++) byte |= (uint32_t)(sh.key16[i0 + q] >= tb) << q;
     }
-    if (j0 + lane < ch.nw) sh.mword[j0 + lane] = mine;
+    uint32_t word = byte << (8 * (lane & 3));
+    word |= __shfl_xor_sync(kFull, word, 1);
+    word |= __shfl_xor_sync(kFull, word, 2);
+    if ((lane & 3) == 0 && (i0 >> 5) < ch.nw) sh.mword[i0 >> 5] = word;
   }
   __syncthreads();
 
