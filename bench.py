@@ -107,6 +107,27 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def needs_l2_flush(working_bytes: int, l2_bytes: int) -> bool:
+    """A working set under four times the L2 size could be partly served from
+    L2 between back-to-back steps: the bench then evicts it before every
+    timed step."""
+    return working_bytes < 4 * l2_bytes
+
+
+def baseline_sample_size(N: int, chunk: int, calib_rate: float, target_s: float):
+    """(chunks, steps) of the CPU-baseline sample: about target_s seconds of
+    oracle time at calib_rate coordinate-steps per second; 14 steps over as
+    many whole chunks as that allows, or every chunk over more steps when the
+    whole layout fits."""
+    nch = -(-N // chunk)
+    work = calib_rate * target_s
+    n_st = 14
+    n_ch = int(work / (n_st * chunk))
+    if n_ch >= nch:
+        n_ch, n_st = nch, max(14, int(work / N))
+    return max(1, n_ch), n_st
+
+
 def alg_bytes(N: int, W: int, K: int) -> dict:
     """Algorithmic (compulsory) HBM bytes of one step, all in the fused step kernel:
     per coordinate W*(2 g + 8 u + 8 e + 1/8 applied mask) + 8 theta + 8 v + 1/8 new mask,
@@ -297,7 +318,7 @@ def run_scape(args, wl, density):
     # writing a buffer of twice the L2 size (untimed); larger ones are not.
     l2_bytes = torch.cuda.get_device_properties(dev).L2_cache_size
     working = sc.info["device_bytes"] + W * N * 2 * n_batches
-    flush = working < 4 * l2_bytes
+    flush = needs_l2_flush(working, l2_bytes)
     scratch = torch.empty(2 * l2_bytes, dtype=torch.uint8, device=dev) if flush else None
 
     def timed(step_fn, steps):
@@ -414,18 +435,11 @@ def run_scape(args, wl, density):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        # sized from a short calibration run (which includes step 0, so it
-        # reads slow) to about 12 s of oracle time:
-        # 14 steps over as many whole chunks as that allows, or, when every
-        # chunk fits, every chunk over as many steps
+        # sized from a short calibration run, which includes step 0 and so
+        # reads slow: a 15 s target lands near 12 s of oracle time
         nch = -(-N // wl.chunk)
         r0, _, _, _ = oracle_sample(wl, density, min(8, nch), 3)
-        work = r0 * 15.0  # coordinate-steps
-        n_st = 14
-        n_ch = int(work / (n_st * wl.chunk))
-        if n_ch >= nch:
-            n_ch, n_st = nch, max(14, int(work / N))
-        n_ch = max(1, n_ch)
+        n_ch, n_st = baseline_sample_size(N, wl.chunk, r0, 15.0)
         rate, dt, n, nc = oracle_sample(wl, density, n_ch, n_st)
         cpu = {"value": rate, "unit": "params/s", "cores": 1, "kind": "oracle",
                "sample": f"{nc} whole chunks ({n} params) of {wl.name}, W={W}, density {density}, "
