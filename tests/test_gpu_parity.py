@@ -152,6 +152,37 @@ def test_tied_bucket_paths(chunk, density, n_high, n_tied, expect_fallback):
         g.close()
 
 
+def test_fallback_on_consecutive_steps():
+    # 6000 residuals tied at |a| = 1.0 per chunk, zero gradients and b1 = 0:
+    # every step keeps k = 655 of them, so the tied bucket stays above the
+    # on-chip list for several steps and the standalone select redoes chunks
+    # on every step (both slots of the step kernel's flagged-chunk counter).
+    wl = synth.tiny(65536 * 2, 2, 65536, 0.01, beta1=0.0)
+    rng = np.random.default_rng(77)
+    e0 = np.full((2, wl.N), 0.5, np.float32)
+    for w in range(2):
+        for c in range(2):
+            pos = c * 65536 + rng.permutation(65536)[:6100]
+            e0[w, pos[:100]] = 2.0
+            e0[w, pos[100:]] = -1.0
+    g, r = DeviceRun(wl, 0.01), OracleRun(wl, 0.01)
+    try:
+        for w in range(2):
+            g.sc.load(E, e0[w], w)
+            r.o.set(oracle.E, e0[w], w)
+        zero = np.zeros((2, wl.N), np.uint16)
+        seen = 0
+        for t in range(6):
+            g.step(zero)
+            r.step(zero)
+            compare(g, r, f"step {t}")
+            n = g.sc._info()["select_fallbacks"]
+            assert n > seen, (t, n, seen)  # this step flagged chunks again
+            seen = n
+    finally:
+        g.close()
+
+
 def test_resume_is_bit_identical():
     wl = synth.tiny(3 * 4096 + 32, 3, 4096, 0.05, seed=8)
     a = DeviceRun(wl, 0.05)
