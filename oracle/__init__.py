@@ -1,7 +1,7 @@
 """SCAPE oracle: plain single-threaded C++ CPU reference of the optimizer step.
 
 TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
-CPU-baseline leg of ``bench.py`` may import this package.  It shares no code
+CPU-baseline and reference legs of ``bench.py`` may import this package.  It shares no code
 with the CUDA path (``sparse_communication_distributed_gb300``) and imports
 nothing from it; its only shared input is the seeded generator in ``synth``.
 

@@ -4,8 +4,8 @@
  * eye.
  *
  * TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the bench's
- * CPU-baseline leg may load this library; the product path never does.  It
- * shares no code, header or helper with the CUDA path.
+ * CPU-baseline and reference legs may load this library; the product path
+ * never does.  It shares no code, header or helper with the CUDA path.
  *
  * Source: "SCAPE: Accurate and Efficient LLM Training with Extreme Sparse
  * Communication" (arXiv 2607.01678): abstract; gist.science technical summary,
