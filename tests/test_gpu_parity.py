@@ -264,6 +264,30 @@ def test_full_size_sampled_chunks(name, density):
     _run_both(wl, density, wl.steps, chunk_ids=ids)
 
 
+def test_full_size_step_host_sampled():
+    # the end-to-end path on the benchmark layout: page-locked host gradients
+    # read in place by the step kernel over the CPU-GPU link
+    wl = synth.WORKLOADS["llama-1.8b-w4"]
+    ids = sample_chunks(wl)
+    g = DeviceRun(wl, 0.01)
+    r = OracleRun(wl, 0.01, chunk_ids=ids)
+    host = [torch.empty(wl.N, dtype=torch.int16).pin_memory() for _ in range(wl.W)]
+    try:
+        for t in range(2):
+            for w in range(wl.W):
+                synth.gpu().grads_into(wl, w, t, g.grads[w])
+                host[w].copy_(g.grads[w])
+            torch.cuda.synchronize()
+            g.sc.step_host(host)
+            g.t += 1
+            r.step()
+            compare(g, r, f"step {t}")
+        check_full_mask(g)
+    finally:
+        g.close()
+        del host
+
+
 # ---- variants: per-tensor chunks, residuals in host memory ---------------------------
 
 from sparse_communication_distributed_gb300.scape import CHUNK_PER_TENSOR, RESIDUAL_HOST  # noqa: E402
