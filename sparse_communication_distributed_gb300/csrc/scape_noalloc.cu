@@ -58,13 +58,19 @@ SCAPE_API int scape_step_noalloc(const scape_step_buffers* b, const void* const*
   if (C < 32 || C > kMaxChunk || C % 32)
     return fail(SCAPE_EINVAL, "chunk %u must be a multiple of 32 in [32, %u]", C, kMaxChunk);
   uint64_t N = 0;
-  for (uint32_t i = 0; i < b->layout->n_tensors; i++) N += b->layout->numel[i];
+  for (uint32_t i = 0; i < b->layout->n_tensors; i++) {
+    if (b->layout->numel[i] > (1ull << 32)) return fail(SCAPE_EINVAL, "tensor too large");
+    N += b->layout->numel[i];
+    if (N >= (1ull << 32)) break;  // rejected below; stops the sum before it can wrap
+  }
   if (N == 0 || N >= (1ull << 32)) return fail(SCAPE_EINVAL, "N must be in [1, 2^32)");
   const uint64_t n_ch = (N + C - 1) / C;
   if (n_ch > kMaxChunks)
     return fail(SCAPE_EINVAL, "%llu chunks exceed the %llu this entry point supports",
                 (unsigned long long)n_ch, (unsigned long long)kMaxChunks);
-  if (!(b->eps > 0.0f)) return fail(SCAPE_EINVAL, "eps must be > 0");
+  if (!std::isfinite(b->beta1) || !std::isfinite(b->beta2) || !std::isfinite(b->lr) ||
+      !std::isfinite(b->wd) || !(b->eps > 0.0f) || !std::isfinite(b->eps))
+    return fail(SCAPE_EINVAL, "hyper-parameters must be finite and eps > 0");
   const uint32_t k_full = (uint32_t)std::floor(b->density * (double)C);
   const uint32_t k_last = (uint32_t)std::floor(b->density * (double)(N - (n_ch - 1) * C));
   const uint64_t K = (n_ch - 1) * (uint64_t)k_full + k_last;

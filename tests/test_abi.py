@@ -105,3 +105,27 @@ def test_injected_allocation_failure_is_reported(lib, monkeypatch):
     assert rc == scape.SCAPE_ENOMEM
     assert not h.value
     assert "allocation" in lib.scape_last_error(None).decode()
+
+
+def _noalloc(lib, numel, hyper=(0.9, 0.95, 1e-3, 0.1, 1e-8), chunk=1024, W=2, density=0.1):
+    # every argument check of scape_step_noalloc runs before any CUDA call, so
+    # null buffers are fine here: the call must fail on the argument first
+    arr = np.asarray(numel, np.uint64)
+    lay = scape._Layout(arr.size, arr.ctypes.data_as(ctypes.POINTER(ctypes.c_uint64)), chunk)
+    b1, b2, lr, wd, eps = hyper
+    sb = scape.StepBuffers(ctypes.pointer(lay), W, density, b1, b2, lr, wd, eps,
+                           None, None, None, None, 0, None, None, None, 0, None, None, 1)
+    return lib.scape_step_noalloc(ctypes.byref(sb), None, None)
+
+
+@pytest.mark.parametrize("numel,hyper,what", [
+    ([(1 << 64) - 1, 2], (0.9, 0.95, 1e-3, 0.1, 1e-8), "tensor too large"),
+    ([1 << 32, 1 << 32], (0.9, 0.95, 1e-3, 0.1, 1e-8), "N must be"),
+    ([1024], (float("nan"), 0.95, 1e-3, 0.1, 1e-8), "hyper-parameters"),
+    ([1024], (0.9, 0.95, float("inf"), 0.1, 1e-8), "hyper-parameters"),
+    ([1024], (0.9, 0.95, 1e-3, 0.1, 0.0), "eps"),
+])
+def test_noalloc_rejects_bad_arguments(lib, numel, hyper, what):
+    assert _noalloc(lib, numel, hyper) == scape.SCAPE_EINVAL
+    assert what in lib.scape_last_error(None).decode()
+
