@@ -10,6 +10,7 @@
 // One thread per 8 consecutive coordinates: W 16-byte gradient loads and two
 // 16-byte loads and stores each of theta, m and v.  HBM traffic per
 // coordinate: 2W + 24 bytes, all compulsory.
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 
@@ -107,7 +108,9 @@ SCAPE_API int scape_dense_adams_step(float* theta, float* m, float* v,
   if (!theta || !m || !v || !aligned16(theta) || !aligned16(m) || !aligned16(v))
     return fail(SCAPE_EINVAL, "theta, m and v must be 16-byte aligned device pointers");
   if (!grad_ptrs) return fail(SCAPE_EINVAL, "grad_ptrs is NULL");
-  if (!(eps > 0.0f)) return fail(SCAPE_EINVAL, "eps must be > 0");
+  if (!std::isfinite(beta1) || !std::isfinite(beta2) || !std::isfinite(lr) ||
+      !std::isfinite(wd) || !(eps > 0.0f) || !std::isfinite(eps))
+    return fail(SCAPE_EINVAL, "hyper-parameters must be finite and eps > 0");
   DenseArgs a{};
   for (int w = 0; w < W; w++) {
     if (!grad_ptrs[w] || !aligned16(grad_ptrs[w]))

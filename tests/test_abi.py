@@ -129,3 +129,17 @@ def test_noalloc_rejects_bad_arguments(lib, numel, hyper, what):
     assert _noalloc(lib, numel, hyper) == scape.SCAPE_EINVAL
     assert what in lib.scape_last_error(None).decode()
 
+
+@pytest.mark.parametrize("hyper", [(float("nan"), 0.95, 1e-3, 0.1, 1e-8),
+                                   (0.9, 0.95, 1e-3, float("inf"), 1e-8),
+                                   (0.9, 0.95, 1e-3, 0.1, 0.0)])
+def test_dense_rejects_bad_hyper_parameters(lib, hyper):
+    # aligned placeholder addresses: the call must fail on the hyper-parameters
+    # before anything touches them or launches
+    fake = ctypes.c_void_p(1 << 20)
+    grads = (ctypes.c_void_p * 2)(1 << 21, 1 << 22)
+    b1, b2, lr, wd, eps = hyper
+    rc = lib.scape_dense_adams_step(fake, fake, fake, grads, 2, 1024, b1, b2, lr, wd, eps, None)
+    assert rc == scape.SCAPE_EINVAL
+    assert "hyper-parameters" in lib.scape_last_error(None).decode()
+
