@@ -13,7 +13,10 @@ torch = pytest.importorskip("torch")
 if not torch.cuda.is_available():
     pytest.skip("needs a CUDA GPU", allow_module_level=True)
 
+import types  # noqa: E402
+
 import synth  # noqa: E402
+from gpu_harness import OracleRun, compare, sample_chunks  # noqa: E402
 from sparse_communication_distributed_gb300 import MASK, THETA, U, V, Scape  # noqa: E402
 from sparse_communication_distributed_gb300 import build as pkg_build  # noqa: E402
 from sparse_communication_distributed_gb300.scape import DEBUG_LIB_PATH  # noqa: E402
@@ -85,3 +88,23 @@ def test_debug_build_records_a_corrupt_mask(debug_lib, monkeypatch):
         assert 8192 <= info["check_where"] < 12288  # the chunk with one bit too many
     finally:
         sc.close()
+
+
+def test_debug_build_full_size_records_nothing(debug_lib):
+    # every guarded index at the benchmark layout's full size (1.8B
+    # coordinates, 27091 chunks): no check fails, and the sampled chunks still
+    # match the oracle bit for bit
+    wl = synth.WORKLOADS["llama-1.8b-w4"]
+    ids = sample_chunks(wl)
+    sc = _run(wl, 0.01, debug_lib, steps=2)
+    r = OracleRun(wl, 0.01, chunk_ids=ids)
+    try:
+        info = sc._info()
+        assert info["checks_compiled"] == 1 and info["check_count"] == 0, info
+        for _ in range(2):
+            r.step()
+        compare(types.SimpleNamespace(sc=sc, wl=wl), r, "debug build, after step 1")
+    finally:
+        sc.close()
+        torch.cuda.empty_cache()
+
