@@ -91,14 +91,14 @@ class Oracle:
 
     def __init__(self, numel, chunk: int, W: int, density: float, beta1=0.9, beta2=0.95,
                  lr=1e-3, wd=0.1, eps=1e-8, chunk_ids=None, lib_path: str = SO,
-                 per_tensor: bool = False):
+                 per_tensor: bool = False, union_mask: bool = False):
         self.lib = load(lib_path)
         numel = np.ascontiguousarray(numel, dtype=np.uint64)
         ids = (np.zeros(0, np.uint64) if chunk_ids is None
                else np.ascontiguousarray(chunk_ids, dtype=np.uint64))
         self.h = self.lib.oracle_create(_p(numel, _u64p), numel.size, chunk, W, density, beta1,
                                         beta2, lr, wd, eps, _p(ids, _u64p), ids.size,
-                                        1 if per_tensor else 0)
+                                        (1 if per_tensor else 0) | (2 if union_mask else 0))
         if not self.h:
             raise ValueError("oracle_create rejected its arguments")
         self.W = W
@@ -122,9 +122,10 @@ class Oracle:
 
     @classmethod
     def for_workload(cls, wl, density: float, chunk_ids=None, lib_path: str = SO,
-                     per_tensor: bool = False):
+                     per_tensor: bool = False, union_mask: bool = False):
         return cls(wl.numel, wl.chunk, wl.W, density, wl.beta1, wl.beta2, wl.lr, wl.wd, wl.eps,
-                   chunk_ids=chunk_ids, lib_path=lib_path, per_tensor=per_tensor)
+                   chunk_ids=chunk_ids, lib_path=lib_path, per_tensor=per_tensor,
+                   union_mask=union_mask)
 
     def __del__(self):
         if getattr(self, "h", None):

@@ -77,6 +77,7 @@ struct Oracle {
   double density = 0;
   float b1 = 0, b2 = 0, lr = 0, wd = 0, eps = 0;
   uint64_t n_chunks_total = 0;
+  bool union_mask = false;            // the non-partitioned variant (union of W top-k)
   std::vector<Chunk> chunks;          // the domain's chunks, ascending
   std::vector<uint64_t> all_start, all_len, all_k;  // every chunk of the layout
   std::vector<uint64_t> dom_index;    // flat index of each domain position
@@ -132,6 +133,29 @@ void partitioned_select(const Oracle& o, const std::vector<float>& a, std::vecto
   }
 }
 
+// The non-partitioned alternative the pages set SCAPE against (technical
+// summary §2, "Partitioned Mask Synchronization": without partitioning, each
+// worker's own top-k lands on different coordinates and the synchronized set
+// fills in): every worker ranks its own accumulator in every chunk with the
+// same key and tie rule, and the mask is the union of the W selections.
+void union_select(const Oracle& o, const std::vector<float>& a, std::vector<uint8_t>& mask) {
+  std::vector<uint8_t> keep;
+  for (const Chunk& c : o.chunks) {
+    uint8_t* m = mask.data() + c.dom0;
+    for (uint32_t i = 0; i < c.len; i++) m[i] = 0;
+    keep.resize(c.len);
+    for (int w = 0; w < o.W; w++) {
+      select_topk(a.data() + (uint64_t)w * o.n + c.dom0, c.len, c.k, keep.data());
+      for (uint32_t i = 0; i < c.len; i++) m[i] |= keep[i];
+    }
+  }
+}
+
+void select_mask(const Oracle& o, const std::vector<float>& a, std::vector<uint8_t>& mask) {
+  if (o.union_mask) union_select(o, a, mask);
+  else partitioned_select(o, a, mask);
+}
+
 void oracle_step_impl(Oracle& o, const uint16_t* grads /* [W][n] */) {
   const uint64_t n = o.n;
   const int W = o.W;
@@ -149,7 +173,7 @@ void oracle_step_impl(Oracle& o, const uint16_t* grads /* [W][n] */) {
         float un = (o.b1 * o.u[x]) + (c1 * g);
         a0[x] = o.e[x] + un;
       }
-    partitioned_select(o, a0, o.mask_prev);
+    select_mask(o, a0, o.mask_prev);
   }
 
   // (1)-(4) on every worker; the kept values are compacted in index order.
@@ -191,8 +215,9 @@ void oracle_step_impl(Oracle& o, const uint16_t* grads /* [W][n] */) {
     o.theta[i] = o.theta[i] - (o.lr * (q + (o.wd * o.theta[i])));   // (7)
   }
 
-  // (8)-(9): next mask from the owners' accumulators; used at step t+1.
-  partitioned_select(o, o.a_last, o.mask_prev);
+  // (8)-(9): next mask from the owners' accumulators (every worker's, in the
+  // union variant); used at step t+1.
+  select_mask(o, o.a_last, o.mask_prev);
   o.t += 1;
 }
 
@@ -202,10 +227,13 @@ enum { OR_THETA = 0, OR_V = 1, OR_U = 2, OR_E = 3, OR_A = 4, OR_B = 5 };
 
 /* Create an oracle for the flat layout of n_tensors tensors (numel[]), chunk
  * size C, W workers.  chunk_ids[0..n_ids) (ascending, distinct) picks the
- * domain; n_ids == 0 means every chunk.  Returns nullptr on bad arguments. */
+ * domain; n_ids == 0 means every chunk.  flags: 1 = chunks restart at every
+ * tensor; 2 = the non-partitioned variant (the mask is the union of every
+ * worker's own top-k in every chunk).  Returns nullptr on bad arguments. */
 OR_API void* oracle_create(const uint64_t* numel, uint32_t n_tensors, uint32_t C, int W,
                            double density, float b1, float b2, float lr, float wd, float eps,
-                           const uint64_t* chunk_ids, uint64_t n_ids, int per_tensor) {
+                           const uint64_t* chunk_ids, uint64_t n_ids, int flags) {
+  const int per_tensor = flags & 1;
   if (!numel || n_tensors == 0 || C == 0 || W < 1 || !(density > 0.0 && density <= 1.0))
     return nullptr;
   Oracle* o = new (std::nothrow) Oracle();
@@ -213,6 +241,7 @@ OR_API void* oracle_create(const uint64_t* numel, uint32_t n_tensors, uint32_t C
   for (uint32_t i = 0; i < n_tensors; i++) o->N += numel[i];
   if (o->N == 0) { delete o; return nullptr; }
   o->C = C; o->W = W; o->density = density;
+  o->union_mask = (flags & 2) != 0;
   o->b1 = b1; o->b2 = b2; o->lr = lr; o->wd = wd; o->eps = eps;
   // Chunk boundaries: every C coordinates of the flat vector, or (per_tensor)
   // every C coordinates of each tensor, its last chunk shorter.

@@ -17,7 +17,9 @@ summary §2 and §3), stated in the oracle header:
   - partitioned top-k: every chunk keeps exactly floor(density*len) entries,
     the largest |a| of its owner, ties to the lower index (checked by its
     characterisation and against numpy's sort);
-  - coordinates never sent only decay: theta *= (1 - lr*wd), v *= b2.
+  - coordinates never sent only decay: theta *= (1 - lr*wd), v *= b2;
+  - the non-partitioned alternative (technical summary §2, "Partitioned Mask
+    Synchronization") keeps the union of every worker's own top-k per chunk.
 """
 from __future__ import annotations
 
@@ -361,11 +363,68 @@ def pin_dense_adams_constant_gradient(lib: str = SO) -> None:
         np.testing.assert_allclose(v, vr, rtol=1e-5)
 
 
+def _union_ref(rows: np.ndarray, k: int) -> np.ndarray:
+    """Union over the rows of each row's top-k by (|a| descending, index
+    ascending), from numpy's lexicographic sort."""
+    n = rows.shape[1]
+    ref = np.zeros(n, bool)
+    for a in rows:
+        order = np.lexsort((np.arange(n), -_key(a).astype(np.int64)))
+        ref[order[:k]] = True
+    return ref
+
+
+def pin_union_mask(lib: str = SO) -> None:
+    """The non-partitioned variant: each chunk's next mask is the union over
+    workers of each worker's own top-k_c (computed here with numpy's sort), so
+    it keeps between k_c and min(len, W*k_c) coordinates and somewhere more
+    than k_c (fill-in); it is applied one step later, and the compact list
+    holds exactly the applied mask's coordinates, ascending."""
+    for kind in (synth.SYN_GAUSS, synth.SYN_STUDENT_Q):
+        wl = synth.tiny(5 * 1024 + 352, 3, 1024, 0.1, kind=kind, seed=5, sigma=2e-3)
+        o = oracle.Oracle.for_workload(wl, 0.1, lib_path=lib, union_mask=True)
+        prev = None
+        grew = False
+        for t in range(3):
+            _run(o, wl, 1, t0=t)
+            m = o.mask(0).astype(bool)
+            used = o.mask(1).astype(bool)
+            if prev is not None:
+                assert np.array_equal(used, prev)
+            idx, _ = o.sparse(0)
+            assert np.array_equal(idx, o.index[used])
+            for j in range(o.chunk_start.size):
+                s, ln = int(o.chunk_start[j]), int(o.chunk_len[j])
+                k = math.floor(0.1 * ln)
+                rows = np.stack([o.get(oracle.A, w)[s:s + ln] for w in range(wl.W)])
+                ref = _union_ref(rows, k)
+                assert np.array_equal(m[s:s + ln], ref), (kind, t, j)
+                cnt = int(ref.sum())
+                assert k <= cnt <= min(ln, wl.W * k)
+                grew |= cnt > k
+            prev = m
+        assert grew
+
+
+def pin_union_single_worker(lib: str = SO) -> None:
+    """With one worker the union is that worker's own top-k: the
+    non-partitioned variant equals the partitioned rule bit for bit."""
+    wl = synth.tiny(3 * 1024 + 96, 1, 1024, 0.05, seed=9)
+    a = oracle.Oracle.for_workload(wl, 0.05, lib_path=lib)
+    b = oracle.Oracle.for_workload(wl, 0.05, lib_path=lib, union_mask=True)
+    for o in (a, b):
+        o.set(oracle.THETA, synth.cpu().theta0(wl, o.index))
+        _run(o, wl, 4)
+    for f in (oracle.THETA, oracle.V, oracle.U, oracle.E):
+        assert np.array_equal(a.get(f).view(np.uint32), b.get(f).view(np.uint32)), f
+    assert np.array_equal(a.mask(0), b.mask(0))
+
+
 ALL_PINS = [
     pin_dense_adams, pin_single_worker_identity, pin_momentum_closed_form, pin_fixed_sum_order,
     pin_accumulator_split, pin_error_feedback_conservation, pin_delayed_mask,
     pin_partitioned_topk, pin_topk_against_sort, pin_shard_geometry, pin_per_tensor_chunks,
     pin_offmask_decay,
     pin_dense_adams_single_worker, pin_dense_adams_matches_scape_density1,
-    pin_dense_adams_constant_gradient,
+    pin_dense_adams_constant_gradient, pin_union_mask, pin_union_single_worker,
 ]

@@ -38,6 +38,13 @@ MUTANTS = [
     ("bias correction added", "float q = bb / (std::sqrt(o.v[i]) + o.eps);",
      "float q = (bb / (1.0f - std::pow(o.b1, (float)(o.t + 1)))) / (std::sqrt(o.v[i]) + o.eps);"),
     ("per-tensor chunks ignore tensor boundaries", "  if (per_tensor) {", "  if (false) {"),
+    ("union: every worker ranks the owner's accumulator",
+     "select_topk(a.data() + (uint64_t)w * o.n + c.dom0, c.len, c.k, keep.data());",
+     "select_topk(a.data() + (uint64_t)c.owner * o.n + c.dom0, c.len, c.k, keep.data());"),
+    ("union: the last worker's selection overwrites", "m[i] |= keep[i];", "m[i] = keep[i];"),
+    ("union: stale bits not cleared", "for (uint32_t i = 0; i < c.len; i++) m[i] = 0;", ""),
+    ("union flag ignored", "if (o.union_mask) union_select(o, a, mask);",
+     "if (false) union_select(o, a, mask);"),
     ("dense: mean misses 1/W", "const float gbar = s * invW;", "const float gbar = s;"),
     ("dense: second moment from the gradient", "v[i] = (b2 * v[i]) + (c2 * (m[i] * m[i]));",
      "v[i] = (b2 * v[i]) + (c2 * (gbar * gbar));"),
