@@ -56,6 +56,8 @@ def parse():
     ap.add_argument("--per-tensor", action="store_true", help="chunks restart at every tensor")
     ap.add_argument("--residual-host", action="store_true",
                     help="keep the residuals in page-locked host memory")
+    ap.add_argument("--union-mask", action="store_true",
+                    help="the non-partitioned variant: the union of every worker's top-k")
     return ap.parse_args()
 
 
@@ -202,7 +204,8 @@ def ncu_traffic(kernel: str, N: int):
     return None, None
 
 
-def oracle_sample(wl, density, n_chunks: int, steps: int, n_batches: int = 2):
+def oracle_sample(wl, density, n_chunks: int, steps: int, n_batches: int = 2,
+                  union_mask: bool = False):
     """Time the oracle (as it stands) on n_chunks whole chunks spread over the
     shards, for ``steps`` steps over ``n_batches`` gradient batches used in
     turn (generated before the timed loop).  Returns (params/s, seconds,
@@ -210,7 +213,7 @@ def oracle_sample(wl, density, n_chunks: int, steps: int, n_batches: int = 2):
     import oracle
     nch = -(-wl.N // wl.chunk)
     ids = np.unique(np.linspace(0, nch - 1, n_chunks).astype(np.int64))
-    o = oracle.Oracle.for_workload(wl, density, chunk_ids=ids)
+    o = oracle.Oracle.for_workload(wl, density, chunk_ids=ids, union_mask=union_mask)
     o.set(oracle.THETA, synth.cpu().theta0(wl, o.index))
     grads = [np.stack([synth.cpu().grads(wl, w, t, idx=o.index) for w in range(wl.W)])
              for t in range(min(n_batches, steps))]
@@ -227,7 +230,7 @@ def run_reference(args, wl, density):
         return
     n_chunks = 16 if wl.N > 1 << 24 else max(1, min(16, -(-wl.N // wl.chunk)))
     steps = args.warmup + args.steps
-    rate, dt, n, nc = oracle_sample(wl, density, n_chunks, steps)
+    rate, dt, n, nc = oracle_sample(wl, density, n_chunks, steps, union_mask=args.union_mask)
     per_step_ms = dt / steps * 1e3
     sample = (f"{nc} whole chunks ({n} params) of {wl.name}, W={wl.W}, density {density}, "
               f"{steps} steps incl. step 0; single-threaded C++ oracle")
@@ -284,8 +287,10 @@ def run_scape(args, wl, density):
     barrier = ranks.barrier
 
     N, W = wl.N, wl.W
-    from sparse_communication_distributed_gb300.scape import CHUNK_PER_TENSOR, RESIDUAL_HOST
-    flags = (CHUNK_PER_TENSOR if args.per_tensor else 0) | (RESIDUAL_HOST if args.residual_host else 0)
+    from sparse_communication_distributed_gb300.scape import (CHUNK_PER_TENSOR, RESIDUAL_HOST,
+                                                              UNION_MASK)
+    flags = ((CHUNK_PER_TENSOR if args.per_tensor else 0) |
+             (RESIDUAL_HOST if args.residual_host else 0) | (UNION_MASK if args.union_mask else 0))
     sc = Scape.for_workload(wl, density, flags=flags)
     K = sc.K
     th = torch.empty(N, dtype=torch.float32, device=dev)
@@ -359,6 +364,8 @@ def run_scape(args, wl, density):
     phases = sc.profile_read()
     sc.profile(False)
     clk = clocks.stop()
+    if args.union_mask:
+        K = sc.K  # the compact count of the last step (it varies with the union's fill-in)
 
     ms_per_step = ranks.max(ms) / args.steps
 
@@ -428,7 +435,8 @@ def run_scape(args, wl, density):
                  "alg_bytes_per_step": d_bytes, "achieved_gbs": d_bytes / (d_ms * 1e-3) / 1e9,
                  "exchange_bytes_per_worker": {
                      "dense_allreduce_fp32": 4 * N,
-                     "scape_sparse_fp32_plus_mask": 4 * K + N // (8 * W)},
+                     "scape_sparse_fp32_plus_mask":
+                         4 * K + (N // 8 if args.union_mask else N // (8 * W))},
                  "note": "one GPU: both steps' exchanges are emulated in HBM, so this compares "
                          "memory work, not network time"}
         del th_d, m_d, v_d
@@ -438,9 +446,9 @@ def run_scape(args, wl, density):
         # sized from a short calibration run, which includes step 0 and so
         # reads slow: a 15 s target lands near 12 s of oracle time
         nch = -(-N // wl.chunk)
-        r0, _, _, _ = oracle_sample(wl, density, min(8, nch), 3)
+        r0, _, _, _ = oracle_sample(wl, density, min(8, nch), 3, union_mask=args.union_mask)
         n_ch, n_st = baseline_sample_size(N, wl.chunk, r0, 15.0)
-        rate, dt, n, nc = oracle_sample(wl, density, n_ch, n_st)
+        rate, dt, n, nc = oracle_sample(wl, density, n_ch, n_st, union_mask=args.union_mask)
         cpu = {"value": rate, "unit": "params/s", "cores": 1, "kind": "oracle",
                "sample": f"{nc} whole chunks ({n} params) of {wl.name}, W={W}, density {density}, "
                          f"{n_st} steps incl. step 0 over 2 gradient batches, {dt:.1f} s of "
@@ -461,6 +469,8 @@ def run_scape(args, wl, density):
     peak, peak_kind = measured_peak()
     ab = alg_bytes(N, W, K)
     traffic, traffic_src = ncu_traffic("step_chunks", N)
+    if args.union_mask:  # the counters were captured on the partitioned kernel
+        traffic, traffic_src = None, None
     a_ms, a_n = phases["step"]
     a_launch_ms = a_ms / max(a_n, 1)
     achieved = ab["step"] / (a_launch_ms * 1e-3) / 1e9
@@ -483,6 +493,8 @@ def run_scape(args, wl, density):
                    "K": K, "grad_dtype": "bf16", "grad_batches": n_batches,
                    "chunking": "per-tensor" if args.per_tensor else "flat",
                    "residuals": "host (page-locked)" if args.residual_host else "HBM",
+                   "mask": ("union of every worker's top-k (non-partitioned)" if args.union_mask
+                            else "partitioned (SCAPE)"),
                    "parallelism": "replicas" if world > 1 else "single GPU, W emulated workers",
                    "l2": (f"flushed before every timed step ({2 * l2_bytes >> 20} MB written, "
                           f"untimed): {working / 1e6:.0f} MB working set" if flush else

@@ -101,7 +101,17 @@ enum {
    * CPU-GPU link: W*N*4 bytes less device memory, at the link's bandwidth.
    * The SCAPE pages offload residual buffers to CPU memory (technical summary
    * §2 "Memory Optimization", §4). */
-  SCAPE_RESIDUAL_HOST = 2u
+  SCAPE_RESIDUAL_HOST = 2u,
+  /* The non-partitioned alternative that SCAPE replaces (technical summary
+   * §2 "Partitioned Mask Synchronization"): in every chunk each worker keeps
+   * the top-k_c of its own |a_w| (same key and tie rule) and M_t is the union
+   * of the W selections, so a chunk keeps between k_c and min(len, W * k_c)
+   * coordinates ("fill-in").  The compact buffers then hold as many values
+   * per worker as the applied mask has bits: K of scape_info and the total
+   * of scape_read_sparse change from step to step (at most
+   * sum_c min(len_c, W * k_c), which the buffers are sized for).  A loaded
+   * mask must keep between k_c and min(len, W * k_c) bits per chunk. */
+  SCAPE_UNION_MASK = 4u
 };
 
 typedef struct {
@@ -112,7 +122,7 @@ typedef struct {
   uint64_t chunks_per_worker; /* q */
   uint32_t k_full;     /* k of a full chunk */
   uint32_t k_last;     /* k of the last chunk */
-  uint64_t K;          /* values per worker per step */
+  uint64_t K;          /* values per worker per step (SCAPE_UNION_MASK: in the last step) */
   uint64_t mask_words; /* ceil(N / 32) */
   int64_t step;        /* steps taken (t) */
   uint64_t device_bytes; /* device memory held by the handle */
@@ -139,7 +149,8 @@ typedef struct {
 int scape_create(const scape_layout* layout, int W, double density, float beta1, float beta2,
                  float lr, float wd, float eps, scape_handle** out);
 
-/* scape_create with options (SCAPE_CHUNK_PER_TENSOR, SCAPE_RESIDUAL_HOST);
+/* scape_create with options (SCAPE_CHUNK_PER_TENSOR, SCAPE_RESIDUAL_HOST,
+ * SCAPE_UNION_MASK, combinable);
  * flags = 0 is scape_create.  k_full and k_last of scape_info are then
  * floor(density * C) and the last chunk's k. */
 int scape_create_ex(const scape_layout* layout, int W, double density, float beta1, float beta2,

@@ -121,8 +121,9 @@ __device__ __forceinline__ Shared carve(unsigned char* s) {
 
 struct Chunk {
   uint64_t c, c0, base;  // index, first coordinate, first packed position
-  uint32_t L, k, nw;     // length, kept count, mask words
-  int owner;
+  uint32_t L, k, nw;     // length, coordinates to select, mask words
+  uint32_t cap;          // compact slots of the chunk: k, or M_{t-1}'s count (union variant)
+  int owner;             // the worker whose accumulator is ranked
 };
 
 enum { PASS_OTHER = 0, PASS_OWNER = 1, PASS_BOOT = 2 };
@@ -164,7 +165,7 @@ __device__ __forceinline__ void stream_worker(const FusedArgs& p, const Shared& 
     do {                                                                  \
       const uint32_t r_ = rank0 + __popc(byte & ((1u << (jj)) - 1u));     \
       if (r_ - tile0 < 32u) stage[r_ - tile0] = (bval);                   \
-      else if (SCAPE_CHECK(p.dbg, r_ < ch.k, CHK_VALS_WRITE,              \
+      else if (SCAPE_CHECK(p.dbg, r_ < ch.cap, CHK_VALS_WRITE,              \
                            ch.c0 + i0 + (jj))) vals[r_] = (bval);         \
     } while (0)
     if (!active) {
@@ -233,7 +234,7 @@ __device__ __forceinline__ void stream_worker(const FusedArgs& p, const Shared& 
     if (WRITE) {
       const uint32_t cnt = __reduce_add_sync(kFull, (uint32_t)__popc(byte));
       __syncwarp();
-      if (lane < cnt && SCAPE_CHECK(p.dbg, tile0 + lane < ch.k, CHK_VALS_STAGE, ch.c0 + t * 256))
+      if (lane < cnt && SCAPE_CHECK(p.dbg, tile0 + lane < ch.cap, CHK_VALS_STAGE, ch.c0 + t * 256))
         vals[tile0 + lane] = stage[lane];
       __syncwarp();
     }
@@ -281,7 +282,7 @@ __device__ __forceinline__ void stream_worker_contig(const FusedArgs& p, const S
     do {                                                                            \
       const uint32_t r_ = (nr[h] & 0x0FFFFFFFu) + __popc((nr[h] >> 28) & ((1u << (jj)) - 1u)); \
       if (r_ - tile0 < 32u) stage[r_ - tile0] = (bval);                             \
-      else if (SCAPE_CHECK(p.dbg, r_ < ch.k, CHK_VALS_WRITE,                        \
+      else if (SCAPE_CHECK(p.dbg, r_ < ch.cap, CHK_VALS_WRITE,                        \
                            ch.c0 + ia + (h) * 128 + (jj))) vals[r_] = (bval);       \
     } while (0)
 #pragma unroll
@@ -344,7 +345,7 @@ __device__ __forceinline__ void stream_worker_contig(const FusedArgs& p, const S
     if (WRITE) {
       const uint32_t cnt = __reduce_add_sync(kFull, (uint32_t)(__popc(nr[0] >> 28) + __popc(nr[1] >> 28)));
       __syncwarp();
-      if (lane < cnt && SCAPE_CHECK(p.dbg, tile0 + lane < ch.k, CHK_VALS_STAGE, ch.c0 + t * 256))
+      if (lane < cnt && SCAPE_CHECK(p.dbg, tile0 + lane < ch.cap, CHK_VALS_STAGE, ch.c0 + t * 256))
         vals[tile0 + lane] = stage[lane];
       __syncwarp();
     }
@@ -366,7 +367,7 @@ __device__ __forceinline__ uint32_t owner_key(const FusedArgs& p, const Shared& 
   float a;
   if ((word >> bit) & 1u) {
     const uint32_t r = sh.wpre[j] + __popc(word & ((1u << bit) - 1u));
-    a = SCAPE_CHECK(p.dbg, r < ch.k, CHK_OWNER_KEY, ch.c0 + i)
+    a = SCAPE_CHECK(p.dbg, r < ch.cap, CHK_OWNER_KEY, ch.c0 + i)
             ? p.vals[(uint64_t)ch.owner * p.Kp + ch.base + r]
             : 0.0f;
   } else {
@@ -622,7 +623,7 @@ __device__ __forceinline__ void update_chunk(const FusedArgs& p, const Shared& s
     for (uint32_t r0 = 0; r0 < cnt; r0 += 32) {
       float mine = 0.0f;
       if (r0 + lane < cnt &&
-          SCAPE_CHECK(p.dbg, tile0 + r0 + lane < ch.k, CHK_BBAR, ch.c0 + t * 256)) {
+          SCAPE_CHECK(p.dbg, tile0 + r0 + lane < ch.cap, CHK_BBAR, ch.c0 + t * 256)) {
         mine = ordered_sum(p, R0 + r0 + lane) * invW;
         p.bbar[R0 + r0 + lane] = mine;
       }
@@ -655,7 +656,7 @@ __device__ __forceinline__ void update_chunk(const FusedArgs& p, const Shared& s
       const bool m = (byte >> jj) & 1u;
       if (m) {
         const uint32_t r = local0 + __popc(byte & ((1u << jj) - 1u));
-        if (SCAPE_CHECK(p.dbg, r < ch.k, CHK_IDX, ch.c0 + i0 + jj))
+        if (SCAPE_CHECK(p.dbg, r < ch.cap, CHK_IDX, ch.c0 + i0 + jj))
           p.idx[ch.base + r] = (uint32_t)(ch.c0 + i0 + jj);
       }
       const float vn = (b2 * vo[jj]) + (c2 * (bb[jj] * bb[jj]));
@@ -686,8 +687,29 @@ __device__ __forceinline__ void stream_pass(const FusedArgs& p, const Shared& sh
   else stream_worker<K, PASS>(p, sh, ch, w);
 }
 
-// CONTIG: residual rows in mapped host memory (whole-sector access mapping)
-template <class K, bool CONTIG>
+// The selection's outcome for the chunk: its mask words into M_t (OR-ed into
+// what the earlier workers selected when "merge"), or a flag for the
+// standalone select, which then redoes the whole chunk.
+template <int NT>
+__device__ __forceinline__ void publish_mask(const FusedArgs& p, const Shared& sh,
+                                             const Chunk& ch, bool ok, bool merge) {
+  const int tid = threadIdx.x;
+  if (ok) {
+    uint32_t* mo = p.mout + ch.c0 / 32;
+    for (uint32_t j = tid; j < ch.nw; j += NT) mo[j] = merge ? (mo[j] | sh.mword[j]) : sh.mword[j];
+  } else if (tid == 0) {
+    p.fallback[ch.c] = 1u;
+    atomicAdd(p.n_fallback, 1u);
+    if (p.pending) atomicAdd(p.pending, 1u);
+  }
+}
+
+// CONTIG: residual rows in mapped host memory (whole-sector access mapping).
+// UNION: the non-partitioned variant: in every chunk each worker's own
+// accumulator is ranked in turn (its pass keeps its keys) and M_t is the
+// union of the W selections; the compact buffers follow M_{t-1}'s per-chunk
+// counts (cbase) instead of k_c.
+template <class K, bool CONTIG, bool UNION>
 __global__ __launch_bounds__(K::NT, K::MINB) void step_chunks(const FusedArgs p) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   const Shared sh = carve<K>(smem_raw);
@@ -710,6 +732,11 @@ __global__ __launch_bounds__(K::NT, K::MINB) void step_chunks(const FusedArgs p)
       ch.L = (uint32_t)((p.N - ch.c0) < p.C ? (p.N - ch.c0) : p.C);
       ch.k = (c == p.n_ch - 1) ? p.k_last : p.k_full;
       ch.base = c * (uint64_t)p.k_full;
+    }
+    ch.cap = ch.k;
+    if (UNION) {
+      ch.base = p.cbase ? p.cbase[c] : 0;
+      ch.cap = p.cbase ? (uint32_t)(p.cbase[c + 1] - p.cbase[c]) : 0u;
     }
     ch.nw = (ch.L + 31) / 32;
     ch.owner = (int)(c / p.q);
@@ -738,60 +765,76 @@ __global__ __launch_bounds__(K::NT, K::MINB) void step_chunks(const FusedArgs p)
     }
 
     if (p.boot) {
-      // step 0, first launch: M_{-1} of this chunk from the owner's step-0
-      // accumulator (read only), ranked on chip like M_t below
-      stream_pass<K, PASS_BOOT, CONTIG>(p, sh, ch, ch.owner);
-      __syncthreads();
-      const bool ok = select_chunk<K>(p, sh, ch);
-      if (ok) {
-        uint32_t* mo = p.mout + ch.c0 / 32;
-        for (uint32_t j = tid; j < ch.nw; j += K::NT) mo[j] = sh.mword[j];
-      } else if (tid == 0) {
-        p.fallback[c] = 1u;
-        atomicAdd(p.n_fallback, 1u);
-        if (p.pending) atomicAdd(p.pending, 1u);
+      // step 0, first launch: M_{-1} of this chunk from the step-0
+      // accumulators (read only), ranked on chip like M_t below: the
+      // owner's, or every worker's in turn in the union variant
+      const int wa = UNION ? 0 : ch.owner, wb = UNION ? p.W : ch.owner + 1;
+      for (int w = wa; w < wb; w++) {
+        Chunk cw = ch;
+        cw.owner = w;
+        stream_pass<K, PASS_BOOT, CONTIG>(p, sh, cw, w);
+        __syncthreads();
+        publish_mask<K::NT>(p, sh, cw, select_chunk<K>(p, sh, cw), w > wa);
+        for (int i = tid; i < 4096; i += K::NT) sh.hist[i] = 0;  // the next worker's
+        __syncthreads();
       }
-      __syncthreads();
       continue;
     }
 
-    // phase 1: the owner's pass, keeping its keys
-    stream_pass<K, PASS_OWNER, CONTIG>(p, sh, ch, ch.owner);
-    if (p.W > 1) prefetch_worker_tile(p, ch.c0, ch.L, ch.owner == 0 ? 1 : 0);
-    __syncthreads();
-
-    // phase 2: top-k of the owner's |a| -> mask words of M_t
-    const bool ok = select_chunk<K>(p, sh, ch);
-    if (ok) {
-      uint32_t* mo = p.mout + ch.c0 / 32;
-      for (uint32_t j = tid; j < ch.nw; j += K::NT) mo[j] = sh.mword[j];
-    } else if (tid == 0) {
-      p.fallback[c] = 1u;
-      atomicAdd(p.n_fallback, 1u);
-      if (p.pending) atomicAdd(p.pending, 1u);
-    }
-
-    // phase 3: every other worker
-    for (int w = 0; w < p.W; w++)
-      if (w != ch.owner) stream_pass<K, PASS_OTHER, CONTIG>(p, sh, ch, w);
-    {
-      const uint32_t i0 = (tid >> 5) * 256 + (tid & 31) * 8;
-      if (i0 + 8 <= ch.L) {
-        prefetch_l2(p.theta + ch.c0 + i0);
-        prefetch_l2(p.v + ch.c0 + i0);
+    if (UNION) {
+      for (int w = 0; w < p.W; w++) {
+        Chunk cw = ch;
+        cw.owner = w;
+        // phase 1 for worker w: its pass, keeping its keys
+        stream_pass<K, PASS_OWNER, CONTIG>(p, sh, cw, w);
+        if (w + 1 < p.W) {
+          prefetch_worker_tile(p, ch.c0, ch.L, w + 1);
+        } else {
+          const uint32_t i0 = (tid >> 5) * 256 + (tid & 31) * 8;
+          if (i0 + 8 <= ch.L) {
+            prefetch_l2(p.theta + ch.c0 + i0);
+            prefetch_l2(p.v + ch.c0 + i0);
+          }
+        }
+        __syncthreads();
+        // phase 2 for worker w: its top-k, OR-ed into M_t
+        publish_mask<K::NT>(p, sh, cw, select_chunk<K>(p, sh, cw), w > 0);
+        for (int i = tid; i < 4096; i += K::NT) sh.hist[i] = 0;  // the next worker's
+        __syncthreads();
       }
-    }
-    __syncthreads();
+      // phase 4: synchronized buffer, second moment, parameters
+      update_chunk<K>(p, sh, ch);
+    } else {
+      // phase 1: the owner's pass, keeping its keys
+      stream_pass<K, PASS_OWNER, CONTIG>(p, sh, ch, ch.owner);
+      if (p.W > 1) prefetch_worker_tile(p, ch.c0, ch.L, ch.owner == 0 ? 1 : 0);
+      __syncthreads();
 
-    // phase 4: synchronized buffer, second moment, parameters
-    update_chunk<K>(p, sh, ch);
+      // phase 2: top-k of the owner's |a| -> mask words of M_t
+      publish_mask<K::NT>(p, sh, ch, select_chunk<K>(p, sh, ch), false);
+
+      // phase 3: every other worker
+      for (int w = 0; w < p.W; w++)
+        if (w != ch.owner) stream_pass<K, PASS_OTHER, CONTIG>(p, sh, ch, w);
+      {
+        const uint32_t i0 = (tid >> 5) * 256 + (tid & 31) * 8;
+        if (i0 + 8 <= ch.L) {
+          prefetch_l2(p.theta + ch.c0 + i0);
+          prefetch_l2(p.v + ch.c0 + i0);
+        }
+      }
+      __syncthreads();
+
+      // phase 4: synchronized buffer, second moment, parameters
+      update_chunk<K>(p, sh, ch);
+    }
     {
       const uint64_t cn = c + gridDim.x;
       if (cn < p.n_ch && !p.chunks && !p.boot) {
         const uint64_t c0n = cn * p.C;
         const uint32_t Ln = (uint32_t)((p.N - c0n) < p.C ? (p.N - c0n) : p.C);
         if ((uint32_t)tid * 2 < (Ln + 31) / 32) prefetch_l2(p.mprev + c0n / 32 + tid * 2);
-        prefetch_worker_tile(p, c0n, Ln, (int)(cn / p.q));
+        prefetch_worker_tile(p, c0n, Ln, UNION ? 0 : (int)(cn / p.q));
       }
     }
     __syncthreads();
@@ -803,7 +846,7 @@ __global__ __launch_bounds__(K::NT, K::MINB) void step_chunks(const FusedArgs p)
 namespace {
 
 // The shared-memory opt-in is per device and per instantiation.
-template <class K, bool CONTIG>
+template <class K, bool CONTIG, bool UNION>
 cudaError_t launch_shape(const FusedArgs& a, cudaStream_t s) {
   static std::atomic<uint64_t> configured{0};
   int dev = 0;
@@ -811,7 +854,7 @@ cudaError_t launch_shape(const FusedArgs& a, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   const uint64_t bit = dev < 64 ? (1ull << dev) : 0ull;  // devices past 64: set every launch
   if (!(configured.load() & bit)) {
-    e = cudaFuncSetAttribute(step_chunks<K, CONTIG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(step_chunks<K, CONTIG, UNION>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)K::SmemBytes);
     if (e != cudaSuccess) return e;
     configured.fetch_or(bit);
@@ -833,7 +876,14 @@ cudaError_t launch_shape(const FusedArgs& a, cudaStream_t s) {
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, step_chunks<K, CONTIG>, a);
+  return cudaLaunchKernelEx(&cfg, step_chunks<K, CONTIG, UNION>, a);
+}
+
+template <class K>
+cudaError_t launch_variant(const FusedArgs& a, cudaStream_t s) {
+  if (a.union_mask)
+    return a.e_host ? launch_shape<K, true, true>(a, s) : launch_shape<K, false, true>(a, s);
+  return a.e_host ? launch_shape<K, true, false>(a, s) : launch_shape<K, false, false>(a, s);
 }
 
 }  // namespace
@@ -841,10 +891,7 @@ cudaError_t launch_shape(const FusedArgs& a, cudaStream_t s) {
 // Chunks of up to 16384 coordinates take the two-CTAs-per-SM shape; every
 // chunk of the handle is at most C long (per-tensor chunks too).
 cudaError_t launch_step_chunks(const FusedArgs& a, cudaStream_t s) {
-  const bool small = a.C <= Small::MAXC;
-  if (a.e_host)
-    return small ? launch_shape<Small, true>(a, s) : launch_shape<Big, true>(a, s);
-  return small ? launch_shape<Small, false>(a, s) : launch_shape<Big, false>(a, s);
+  return a.C <= Small::MAXC ? launch_variant<Small>(a, s) : launch_variant<Big>(a, s);
 }
 
 }  // namespace scape

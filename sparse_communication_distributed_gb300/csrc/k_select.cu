@@ -111,8 +111,11 @@ __device__ __forceinline__ int quad_keys(const SelectArgs& p, const SelectSmem& 
   return nv;
 }
 
+// Ranks worker w's accumulator in chunk c and writes the chunk's mask words
+// (OR-ed into the words already there when "merge": the union variant).
 template <int SRC>
-__device__ void select_one(const SelectArgs& p, SelectSmem& sm, const uint64_t c) {
+__device__ void select_one(const SelectArgs& p, SelectSmem& sm, const uint64_t c, const int w,
+                           const bool merge) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   uint64_t c0, base_c;
   uint32_t L, k;
@@ -128,7 +131,11 @@ __device__ void select_one(const SelectArgs& p, SelectSmem& sm, const uint64_t c
     k = (c == p.n_ch - 1) ? p.k_last : p.k_full;
     base_c = c * (uint64_t)p.k_full;
   }
-  const int w = p.rank_worker > 0 ? p.rank_worker - 1 : (int)(c / p.q);
+  uint32_t kcap = k;  // compact slots of the chunk (M_{t-1}'s count in the union variant)
+  if (p.cbase) {  // the union variant's compact layout
+    base_c = p.cbase[c];
+    kcap = (uint32_t)(p.cbase[c + 1] - p.cbase[c]);
+  }
   const uint32_t nwc = (L + 31) / 32;
   uint32_t* mout = p.mout + c0 / 32;
 
@@ -136,7 +143,7 @@ __device__ void select_one(const SelectArgs& p, SelectSmem& sm, const uint64_t c
     for (uint32_t j = tid; j < nwc; j += kNT) {
       uint32_t word = 0u;
       if (k != 0) word = (j == nwc - 1 && (L & 31)) ? ((1u << (L & 31)) - 1u) : 0xFFFFFFFFu;
-      mout[j] = word;
+      mout[j] = merge ? (mout[j] | word) : word;
     }
     return;
   }
@@ -182,7 +189,7 @@ __device__ void select_one(const SelectArgs& p, SelectSmem& sm, const uint64_t c
       const uint32_t qd = base + lane;
       if (qd < nq) {
         unsigned long long X[4];
-        const int nv = quad_keys<SRC>(p, sm, w, c0, L, k, base_c, qd, X);
+        const int nv = quad_keys<SRC>(p, sm, w, c0, L, kcap, base_c, qd, X);
         for (int s = 0; s < nv; s++)
           if ((X[s] >> (kTB - pbits)) == prefix)
             atomicAdd(&sm.hist[(uint32_t)(X[s] >> shift) & (uint32_t)(nb - 1)], 1u);
@@ -212,7 +219,7 @@ __device__ void select_one(const SelectArgs& p, SelectSmem& sm, const uint64_t c
     unsigned long long Xc[4];
     if (qd < nq) {
       unsigned long long X[4];
-      const int nv = quad_keys<SRC>(p, sm, w, c0, L, k, base_c, qd, X);
+      const int nv = quad_keys<SRC>(p, sm, w, c0, L, kcap, base_c, qd, X);
       for (int s = 0; s < nv; s++) {
         const unsigned long long hi = X[s] >> rem;
         if (resolved ? (hi >= prefix) : (hi > prefix)) nib |= 1u << s;
@@ -232,7 +239,7 @@ __device__ void select_one(const SelectArgs& p, SelectSmem& sm, const uint64_t c
     part |= __shfl_xor_sync(kFull, part, 2);
     part |= __shfl_xor_sync(kFull, part, 4);
     const uint32_t j = (base >> 3) + (lane >> 3);
-    if ((lane & 7) == 0 && j < nwc) mout[j] = part;
+    if ((lane & 7) == 0 && j < nwc) mout[j] = merge ? (mout[j] | part) : part;
   }
   __syncthreads();
 
@@ -281,8 +288,15 @@ __global__ __launch_bounds__(kNT, 2) void select_topk(const SelectArgs p) {
   if (p.pending && *p.pending == 0u) return;  // the step kernel flagged no chunk
   for (uint64_t c = blockIdx.x; c < p.n_ch; c += gridDim.x) {
     if (p.flags && p.flags[c] == 0u) continue;
-    select_one<SRC>(p, sm, c);
-    __syncthreads();
+    if (p.union_mask) {  // the chunk's words: the union of every worker's selection
+      for (int w = 0; w < p.W; w++) {
+        select_one<SRC>(p, sm, c, w, w > 0);
+        __syncthreads();
+      }
+    } else {
+      select_one<SRC>(p, sm, c, p.rank_worker > 0 ? p.rank_worker - 1 : (int)(c / p.q), false);
+      __syncthreads();
+    }
     if (p.flags && threadIdx.x == 0) p.flags[c] = 0u;
   }
 }

@@ -56,7 +56,11 @@ struct scape_handle {
   uint32_t launches = 0;           // step-kernel launches (launch i counts into slot i % 2)
   uint16_t* stage = nullptr;  // scape_step_host staging, W x N bf16
   uint32_t* diag = nullptr;   // scape_mask_stats: two masks + 3 counters (first use)
-  uint32_t flags = 0;         // SCAPE_CHUNK_PER_TENSOR | SCAPE_RESIDUAL_HOST
+  uint32_t flags = 0;         // SCAPE_CHUNK_PER_TENSOR | SCAPE_RESIDUAL_HOST | SCAPE_UNION_MASK
+  // union variant: packed base of every chunk of mask[b] (n_ch + 1 entries;
+  // the last is the mask's total) and the per-chunk counts behind it
+  uint64_t* cbase[2] = {nullptr, nullptr};
+  uint32_t* ccount = nullptr;
   std::vector<ChunkDesc> chunks;     // chunk table (host copy, every mode)
   ChunkDesc* chunks_dev = nullptr;   // device copy, per-tensor mode only
   uint64_t host_bytes = 0;           // page-locked host memory held (residuals)
@@ -119,7 +123,7 @@ cudaError_t dalloc(scape_handle* h, T** p, uint64_t count) {
 void release(scape_handle* h) {
   void* ps[] = {h->theta, h->v, h->u, h->vals, h->bbar, h->idx, h->mask[0], h->mask[1],
                 h->fallback, h->n_fallback, h->stage, h->diag, h->chunks_dev, h->dbg,
-                h->pending};
+                h->pending, h->cbase[0], h->cbase[1], h->ccount};
   for (void* p : ps)
     if (p) cudaFree(p);
   if (h->e) {
@@ -182,8 +186,9 @@ cudaError_t wait_last(scape_handle* h) {
 }
 
 // Checks that a 0/1 bitmap (host copy) carries exactly k_c bits in every chunk
-// and none past N.
+// (in the union variant between k_c and min(len, W * k_c)) and none past N.
 bool mask_valid(const scape_handle* h, const std::vector<uint32_t>& m, std::string& why) {
+  const bool uni = (h->flags & SCAPE_UNION_MASK) != 0;
   for (uint64_t c = 0; c < h->n_ch; c++) {
     const ChunkDesc& d = h->chunks[c];
     const uint64_t w0 = d.start / 32;
@@ -194,9 +199,11 @@ bool mask_valid(const scape_handle* h, const std::vector<uint32_t>& m, std::stri
       if (j == nw - 1 && (d.len & 31)) word &= (1u << (d.len & 31)) - 1u;
       cnt += __builtin_popcount(word);
     }
-    if (cnt != d.k) {
+    const uint64_t hi = uni ? std::min<uint64_t>(d.len, (uint64_t)h->W * d.k) : d.k;
+    if (cnt < d.k || cnt > hi) {
       why = "chunk " + std::to_string(c) + " has " + std::to_string(cnt) + " bits, needs " +
-            std::to_string(d.k);
+            (uni ? "between " + std::to_string(d.k) + " and " + std::to_string(hi)
+                 : std::to_string(d.k));
       return false;
     }
   }
@@ -242,7 +249,7 @@ SCAPE_API int scape_create_ex(const scape_layout* layout, int W, double density,
   if (!std::isfinite(beta1) || !std::isfinite(beta2) || !std::isfinite(lr) ||
       !std::isfinite(wd) || !(eps > 0.0f) || !std::isfinite(eps))
     return fail(nullptr, SCAPE_EINVAL, "hyper-parameters must be finite and eps > 0");
-  if (flags & ~(uint32_t)(SCAPE_CHUNK_PER_TENSOR | SCAPE_RESIDUAL_HOST))
+  if (flags & ~(uint32_t)(SCAPE_CHUNK_PER_TENSOR | SCAPE_RESIDUAL_HOST | SCAPE_UNION_MASK))
     return fail(nullptr, SCAPE_EINVAL, "unknown flags 0x%x", flags);
   if (flags & SCAPE_CHUNK_PER_TENSOR)
     for (uint32_t i = 0; i + 1 < layout->n_tensors; i++)
@@ -293,7 +300,12 @@ SCAPE_API int scape_create_ex(const scape_layout* layout, int W, double density,
   h->q = (h->n_ch + W - 1) / W;
   h->k_full = (uint32_t)std::floor(density * (double)C);
   h->k_last = h->chunks.back().k;
-  h->Kp = (h->K + 3) / 4 * 4;
+  uint64_t kmax = h->K;  // compact values per worker at most
+  if (flags & SCAPE_UNION_MASK) {
+    kmax = 0;
+    for (const ChunkDesc& d : h->chunks) kmax += std::min<uint64_t>(d.len, (uint64_t)W * d.k);
+  }
+  h->Kp = (kmax + 3) / 4 * 4;
 
   cudaError_t e = cudaSuccess;
   if (e == cudaSuccess) e = dalloc(h, &h->theta, h->Np);
@@ -328,6 +340,11 @@ SCAPE_API int scape_create_ex(const scape_layout* layout, int W, double density,
   if (e == cudaSuccess) e = dalloc(h, &h->n_fallback, 1);
   if (e == cudaSuccess) e = dalloc(h, &h->dbg, 4);
   if (e == cudaSuccess) e = dalloc(h, &h->pending, 2);
+  if (flags & SCAPE_UNION_MASK) {
+    if (e == cudaSuccess) e = dalloc(h, &h->cbase[0], h->n_ch + 1);
+    if (e == cudaSuccess) e = dalloc(h, &h->cbase[1], h->n_ch + 1);
+    if (e == cudaSuccess) e = dalloc(h, &h->ccount, h->n_ch);
+  }
   if (e == cudaSuccess && (flags & SCAPE_CHUNK_PER_TENSOR)) {
     e = dalloc(h, &h->chunks_dev, h->n_ch);
     if (e == cudaSuccess)
@@ -364,6 +381,19 @@ SCAPE_API const char* scape_last_error(const scape_handle* h) {
   return h ? h->err.c_str() : g_create_err.c_str();
 }
 
+// Compact values per worker of the last step: sum_c k_c, or in the union
+// variant the count of the mask that step applied (read from the device; the
+// caller has waited for the step).
+static cudaError_t last_K(const scape_handle* h, uint64_t* K) {
+  *K = h->K;
+  if (!(h->flags & SCAPE_UNION_MASK)) return cudaSuccess;
+  if (!h->stepped) {
+    *K = 0;
+    return cudaSuccess;
+  }
+  return cudaMemcpy(K, h->cbase[1 - h->prev] + h->n_ch, sizeof(uint64_t), cudaMemcpyDeviceToHost);
+}
+
 SCAPE_API int scape_info(const scape_handle* h, scape_info_t* out) {
   if (!h || !out) return SCAPE_EINVAL;
   out->N = h->N;
@@ -383,6 +413,7 @@ SCAPE_API int scape_info(const scape_handle* h, scape_info_t* out) {
       cudaMemcpy(&nf, h->n_fallback, 4, cudaMemcpyDeviceToHost) != cudaSuccess)
     return cuda_fail(hm, cudaGetLastError(), "scape_info");
   out->select_fallbacks = nf;
+  if (last_K(h, &out->K) != cudaSuccess) return cuda_fail(hm, cudaGetLastError(), "scape_info");
   out->flags = h->flags;
   out->host_bytes = h->host_bytes;
   uint32_t dbg[4] = {0, 0, 0, 0};
@@ -436,6 +467,10 @@ static void fill_fused(const scape_handle* h, const uint16_t* const* g, const ui
   a.wd = h->wd;
   a.eps = h->eps;
   a.invW = h->invW;
+  if (h->flags & SCAPE_UNION_MASK) {
+    a.union_mask = 1;
+    a.cbase = h->cbase[h->prev];  // bases of M_{t-1}
+  }
 }
 
 // Launch i of the step kernel counts the chunks it flags into pending[i % 2]
@@ -471,6 +506,12 @@ static int step_device(scape_handle* h, const uint16_t* const* g, cudaStream_t s
   sa.k_last = h->k_last;
   sa.chunks = h->chunks_dev;
   sa.dbg = h->dbg;
+  const bool uni = (h->flags & SCAPE_UNION_MASK) != 0;
+  if (uni) {
+    sa.union_mask = 1;
+    sa.W = h->W;
+    sa.cbase = h->cbase[h->prev];  // keys rebuilt from the compact values on M_{t-1}
+  }
 
   // a mask read enqueued by scape_mask_async on another stream must finish
   // before this step overwrites its buffer (M_t here; M_{-1} too at step 0)
@@ -495,6 +536,9 @@ static int step_device(scape_handle* h, const uint16_t* const* g, cudaStream_t s
     sa.mout = mprev;
     sa.flags = h->fallback;
     if ((e = launch_select(sa, true, s)) != cudaSuccess) return cuda_fail(h, e, "select (step 0)");
+    if (uni && (e = launch_chunk_bases(mprev, h->chunks_dev, h->n_ch, h->C, h->N, h->ccount,
+                                       h->cbase[h->prev], s)) != cudaSuccess)
+      return cuda_fail(h, e, "chunk bases (step 0)");
     pt.done();
   }
   {
@@ -510,6 +554,10 @@ static int step_device(scape_handle* h, const uint16_t* const* g, cudaStream_t s
     sa.flags = h->fallback;
     PhaseTimer pt(h, SCAPE_PH_SELECT_FALLBACK, s);
     if ((e = launch_select(sa, false, s)) != cudaSuccess) return cuda_fail(h, e, "select (fallback)");
+    // union variant: the compact layout of M_t, for the next step
+    if (uni && (e = launch_chunk_bases(mcur, h->chunks_dev, h->n_ch, h->C, h->N, h->ccount,
+                                       h->cbase[1 - h->prev], s)) != cudaSuccess)
+      return cuda_fail(h, e, "chunk bases");
     pt.done();
   }
   h->prev = 1 - h->prev;
@@ -693,6 +741,11 @@ SCAPE_API int scape_load_state(scape_handle* h, int which, int w, const void* sr
       return fail(h, SCAPE_EINVAL, "invalid mask: %s", why.c_str());
     if ((e = cudaMemcpy(base, m.data(), count * 4, cudaMemcpyHostToDevice)) != cudaSuccess)
       return cuda_fail(h, e, "scape_load_state");
+    if ((h->flags & SCAPE_UNION_MASK) &&  // the next step's compact layout
+        ((e = launch_chunk_bases(h->mask[h->prev], h->chunks_dev, h->n_ch, h->C, h->N, h->ccount,
+                                 h->cbase[h->prev], nullptr)) != cudaSuccess ||
+         (e = cudaDeviceSynchronize()) != cudaSuccess))
+      return cuda_fail(h, e, "scape_load_state");
     h->has_mask = true;
     return SCAPE_OK;
   }
@@ -704,10 +757,16 @@ SCAPE_API int scape_read_sparse(scape_handle* h, int w, uint32_t* idx, float* va
                                 uint64_t offset, uint64_t count, uint64_t* total) {
   if (!h) return SCAPE_EINVAL;
   if (w < -1 || w >= h->W) return fail(h, SCAPE_EINVAL, "worker %d outside [-1, %d)", w, h->W);
-  if (total) *total = h->K;
-  if (!h->stepped) return fail(h, SCAPE_ESTATE, "no step has run");
-  if (offset > h->K || count > h->K - offset) return fail(h, SCAPE_EINVAL, "range outside [0, K)");
+  if (!h->stepped) {
+    if (total) *total = (h->flags & SCAPE_UNION_MASK) ? 0 : h->K;
+    return fail(h, SCAPE_ESTATE, "no step has run");
+  }
   cudaError_t e = wait_last(h);
+  uint64_t K = h->K;
+  if (e == cudaSuccess) e = last_K(h, &K);
+  if (e != cudaSuccess) return cuda_fail(h, e, "scape_read_sparse");
+  if (total) *total = K;
+  if (offset > K || count > K - offset) return fail(h, SCAPE_EINVAL, "range outside [0, K)");
   if (e == cudaSuccess && idx && count)
     e = cudaMemcpy(idx, h->idx + offset, count * 4, cudaMemcpyDefault);
   if (e == cudaSuccess && vals && count) {
@@ -788,6 +847,7 @@ SCAPE_API int scape_mask_stats(scape_handle* h, scape_mask_stats_t* out) {
   sa.chunks = h->chunks_dev;
   sa.dbg = h->dbg;
   sa.mout = tmp;
+  if (h->flags & SCAPE_UNION_MASK) sa.cbase = h->cbase[1 - h->prev];  // layout of M_{t-1}
   for (int w = 0; w < h->W; w++) {
     sa.rank_worker = w + 1;
     if ((e = launch_select(sa, false, s)) != cudaSuccess) return cuda_fail(h, e, "select");

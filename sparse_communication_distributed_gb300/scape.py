@@ -21,7 +21,7 @@ THETA, V, U, E, MASK, STEP = 0, 1, 2, 3, 4, 5
 PHASES = ("select_boot", "step", "select_fallback", "h2d")
 
 # Symbols declared in include/scape.h (checked by the ABI test).
-CHUNK_PER_TENSOR, RESIDUAL_HOST = 1, 2
+CHUNK_PER_TENSOR, RESIDUAL_HOST, UNION_MASK = 1, 2, 4
 EXPORTS = ("scape_create", "scape_create_ex", "scape_step", "scape_step_host", "scape_mask",
            "scape_mask_async", "scape_destroy",
            "scape_info", "scape_read_state", "scape_load_state", "scape_read_sparse",
@@ -176,6 +176,9 @@ class Scape:
 
     @property
     def K(self) -> int:
+        """Compact values per worker of the last step (fixed unless UNION_MASK)."""
+        if self.info["flags"] & UNION_MASK:
+            return self._info()["K"]
         return self.info["K"]
 
     @property

@@ -73,10 +73,10 @@ class OracleRun:
     generator."""
 
     def __init__(self, wl, density: float, chunk_ids=None, theta0: bool = True,
-                 per_tensor: bool = False):
+                 per_tensor: bool = False, union_mask: bool = False):
         self.wl = wl
         self.o = oracle.Oracle.for_workload(wl, density, chunk_ids=chunk_ids,
-                                            per_tensor=per_tensor)
+                                            per_tensor=per_tensor, union_mask=union_mask)
         if theta0:
             self.o.set(oracle.THETA, synth.cpu().theta0(wl, self.o.index))
         self.t = 0
@@ -155,6 +155,46 @@ def compare_all(g: DeviceRun, r: OracleRun, what: str = "") -> None:
             _, ov = o.sparse(w)
             assert np.array_equal(gi.astype(np.uint64), oidx), f"idx {what}"
             assert_close_exact(f"vals[{w}] {what}", gv, ov)
+
+
+def compare_by_coordinate(g: DeviceRun, r: OracleRun, what: str = "") -> None:
+    """compare() for layouts whose packed positions depend on every chunk (the
+    union variant): state and mask words chunk by chunk over the oracle's
+    chunks, and each chunk's compact entries located through the device's own
+    coordinate list."""
+    o, sc, W = r.o, g.sc, g.wl.W
+    m_gen = o.mask(0)
+    K = sc.K
+    gidx, _ = sc.sparse(0, count=K)
+    gidx = gidx.astype(np.uint64)
+    assert np.all(np.diff(gidx.astype(np.int64)) > 0), f"idx not ascending {what}"
+    g_vals = [sc.sparse(w, count=K)[1] for w in list(range(W)) + [-1]]
+    oidx, _ = o.sparse(0)
+    o_vals = [o.sparse(w)[1] for w in list(range(W)) + [-1]]
+    pos = 0
+    for j in range(o.chunk_start.size):
+        s, ln = int(o.chunk_start[j]), int(o.chunk_len[j])
+        sl = slice(pos, pos + ln)
+        tag = f"{what} chunk at {s}"
+        assert_close_exact(f"theta {tag}", sc.read(THETA, offset=s, count=ln), o.get(oracle.THETA)[sl])
+        assert_close_exact(f"v {tag}", sc.read(V, offset=s, count=ln), o.get(oracle.V)[sl])
+        for w in range(W):
+            assert_close_exact(f"u[{w}] {tag}", sc.read(U, w, offset=s, count=ln),
+                               o.get(oracle.U, w)[sl])
+            assert_close_exact(f"e[{w}] {tag}", sc.read(E, w, offset=s, count=ln),
+                               o.get(oracle.E, w)[sl])
+        nw = (ln + 31) // 32
+        words = sc.read(MASK, offset=s // 32, count=nw)
+        ref = oracle.pack_bits(m_gen[sl])
+        if not np.array_equal(words, ref):
+            bad = np.nonzero(words != ref)[0]
+            raise AssertionError(f"mask {tag}: {bad.size} words differ, first word {bad[0]}")
+        ga, gb = np.searchsorted(gidx, [s, s + ln])
+        oa, ob = np.searchsorted(oidx, [s, s + ln])
+        assert np.array_equal(gidx[ga:gb], oidx[oa:ob]), f"idx {tag}"
+        for gv, ov, w in zip(g_vals, o_vals, list(range(W)) + [-1]):
+            assert_close_exact(f"vals[{w}] {tag}", gv[ga:gb], ov[oa:ob])
+        pos += ln
 
 
 def sample_chunks(wl, n_extra: int = 4, seed: int = 0) -> list[int]:
