@@ -357,7 +357,7 @@ def _random_case(seed):
     return wl, density, per_tensor
 
 
-@pytest.mark.parametrize("seed", range(12))
+@pytest.mark.parametrize("seed", list(range(12)) + list(range(100, 112)))
 def test_random_shapes(seed):
     wl, density, per_tensor = _random_case(seed)
     g = DeviceRun(wl, density, flags=CHUNK_PER_TENSOR if per_tensor else 0)

@@ -135,7 +135,7 @@ def test_union_mask_load_and_diagnostics():
         g.close()
 
 
-@pytest.mark.parametrize("seed", range(18, 24))
+@pytest.mark.parametrize("seed", list(range(18, 24)) + list(range(200, 206)))
 def test_union_random_shapes(seed):
     rng = np.random.default_rng(2000 + seed)
     W = int(rng.integers(1, 10))
