@@ -8,7 +8,8 @@
 // it before moving to the next chunk, so each state array is streamed through
 // HBM exactly once per step and the selection runs on-chip.
 //
-// Phases per chunk (1024 threads, ~180 KB of shared memory, one CTA per SM):
+// Phases per chunk (one 1024-thread CTA per SM with 188.8 KB of shared memory;
+// chunks of at most 16384 coordinates: two 512-thread CTAs per SM):
 //  0. load the chunk's words of M_{t-1} and their exclusive popcount prefix:
 //     the packed position of a kept coordinate i is
 //       base_c + popcount(M_{t-1} bits of the chunk before i),
@@ -37,6 +38,12 @@
 // At step 0 a first launch in boot mode builds M_{-1} the same way: phases 1
 // and 2 on the owner's step-0 accumulator a = e + (b1*u + c1*g), computed
 // read-only, with nothing else written.
+// The union variant (the non-partitioned alternative) runs phases 1 and 2 for
+// every worker of the chunk in turn, OR-ing the W selections into M_t, and
+// takes base_c from the prefix of M_{t-1}'s per-chunk counts.
+// The grid is persistent and balanced (the fewest rounds, the last one as
+// full as possible); launches use programmatic dependent launch, and the
+// count of chunks left to the standalone select lives in a two-slot ring.
 // Arithmetic is the fp32 rule of the library header, with the same
 // parenthesisation and no FMA contraction (built with -fmad=false).
 //
