@@ -304,6 +304,8 @@ int scape_dense_adams_step(float* theta, float* m, float* v, const void* const* 
  *   vals            W rows of K fp32 (row stride vals_stride >= K): kept values
  *   bbar, idx       K fp32 / K uint32: synchronized buffer and its coordinates
  * K = sum over chunks of floor(density * chunk length), as scape_info gives.
+ * The step is the partitioned rule on flat chunks (scape_create with no
+ * options): no per-tensor chunks, host-resident residuals or union variant.
  * first_step != 0 means there is no M_{t-1} yet: the call first writes the
  * step-0 mask into mask_prev, as scape_step does on a new handle.  Between
  * calls the caller swaps mask_prev and mask_next.
