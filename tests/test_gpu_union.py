@@ -149,3 +149,34 @@ def test_union_random_shapes(seed):
                         sigma=1e-3, seed=seed)
     _run(wl, density, 3, flags=UNION_MASK | (CHUNK_PER_TENSOR if per_tensor else 0),
          per_tensor=per_tensor)
+
+
+def test_union_debug_build_records_nothing():
+    # the debug build's guards bound every compact slot by the chunk's count in
+    # M_{t-1} (the union's capacity): on valid input none fires and the result
+    # equals the release build's bit for bit
+    import os
+    from sparse_communication_distributed_gb300 import build as pkg_build
+    from sparse_communication_distributed_gb300.scape import DEBUG_LIB_PATH, Scape
+    if not os.path.exists(DEBUG_LIB_PATH):
+        pkg_build.build(debug_checks=True)
+    wl = synth.tiny(3 * 65536 + 96, 4, 65536, 0.01, seed=77)
+    dev = torch.device("cuda")
+    out = []
+    for lib in (None, DEBUG_LIB_PATH):
+        kw = {} if lib is None else {"lib_path": lib}
+        sc = Scape.for_workload(wl, 0.01, flags=UNION_MASK, **kw)
+        grads = [torch.empty(wl.N, dtype=torch.int16, device=dev) for _ in range(wl.W)]
+        for t in range(3):
+            for w in range(wl.W):
+                synth.gpu().grads_into(wl, w, t, grads[w])
+            sc.step(grads)
+        torch.cuda.synchronize()
+        info = sc._info()
+        out.append((sc.read(THETA).view(np.uint32), sc.read(MASK), sc.sparse(-1)[1].view(np.uint32),
+                    info))
+        sc.close()
+    (th_r, m_r, b_r, _), (th_d, m_d, b_d, info_d) = out
+    assert info_d["checks_compiled"] == 1 and info_d["check_count"] == 0, info_d
+    assert np.array_equal(th_r, th_d) and np.array_equal(m_r, m_d) and np.array_equal(b_r, b_d)
+
