@@ -43,11 +43,16 @@ def _run(wl, density, steps, flags=UNION_MASK, chunk_ids=None, per_tensor=False)
     (3 * 65536 + 96, 4, 65536, 0.01),      # 1024-thread shape
     (70001, 5, 1024, 0.02),                # odd sizes
     (4099, 9, 96, 0.2),                    # W * k_c above the chunk length: capped at len
+    (2048 + 7, 4, 512, 1.0),               # density 1: every worker keeps everything
 ])
 def test_union_every_coordinate(N, W, chunk, density):
     ks = _run(synth.tiny(N, W, chunk, density, seed=N), density, 4)
     k_sum = sum(int(np.floor(density * min(chunk, N - c))) for c in range(0, N, chunk))
-    assert all(k >= k_sum for k in ks) and max(ks) > k_sum  # the union fills in
+    assert all(k >= k_sum for k in ks)
+    if density < 1.0:
+        assert max(ks) > k_sum  # the union fills in
+    else:
+        assert ks == [N] * len(ks)
 
 
 def test_union_single_worker_equals_partitioned():
