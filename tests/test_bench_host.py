@@ -62,3 +62,20 @@ def test_baseline_sample_size():
     assert bench.baseline_sample_size(1 << 20, 4096, 7.9e6, 15.0) == (256, 113)
     # never below 14 steps or one chunk
     assert bench.baseline_sample_size(1 << 20, 4096, 1.0, 15.0) == (1, 14)
+
+
+def test_clock_parse_and_throttle_rule():
+    lines = "\n".join([
+        "2070, 2070, 900.1, Not Active, Not Active, Not Active, Not Active",
+        "2055, 2070, 1100.5, Not Active, Not Active, Not Active, Active",
+        "2070, 2070, 1200.0, Not Active, Not Active, Not Active, Not Active",
+        "garbage line",
+    ])
+    c = bench.ClockSampler.parse(lines)
+    assert c["sm_mhz"] == 2070 and c["sm_max_mhz"] == 2070 and c["samples"] == 3
+    assert c["reasons"] == ["sw_power_cap"]
+    assert not (bench.THROTTLED & set(c["reasons"]))  # a power cap is only noted
+    c = bench.ClockSampler.parse("1800, 2070, 1300, Active, Not Active, Not Active, Not Active")
+    assert bench.THROTTLED & set(c["reasons"]) == {"hw_slowdown"}  # re-measured
+    assert bench.ClockSampler.parse("") is None
+
