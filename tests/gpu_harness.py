@@ -9,12 +9,15 @@ coordinate lists and counts must be bit-exact.
 """
 from __future__ import annotations
 
+import os
+
 import numpy as np
 import torch
 
 import oracle
 import synth
 from sparse_communication_distributed_gb300 import E, MASK, THETA, U, V, Scape
+from sparse_communication_distributed_gb300.scape import DEBUG_LIB_PATH
 
 RTOL, ATOL = 1e-6, 1e-12
 
@@ -41,7 +44,11 @@ class DeviceRun:
 
     def __init__(self, wl, density: float, theta0: bool = True, flags: int = 0):
         self.wl = wl
-        self.sc = Scape.for_workload(wl, density, flags=flags)
+        # SCAPE_TEST_LIB=debug runs the suite on libscape_debug.so, whose kernels
+        # check every mask-dependent index; close() then asserts none failed
+        self.debug = os.environ.get("SCAPE_TEST_LIB") == "debug"
+        lib = {"lib_path": DEBUG_LIB_PATH} if self.debug else {}
+        self.sc = Scape.for_workload(wl, density, flags=flags, **lib)
         self.dev = torch.device("cuda")
         self.grads = [torch.empty(wl.N, dtype=torch.int16, device=self.dev) for _ in range(wl.W)]
         if theta0:
@@ -63,6 +70,9 @@ class DeviceRun:
         self.t += 1
 
     def close(self):
+        if self.debug:
+            info = self.sc._info()
+            assert info["checks_compiled"] == 1 and info["check_count"] == 0, info
         self.sc.close()
         self.grads = None
         torch.cuda.empty_cache()
