@@ -411,15 +411,27 @@ def run_scape(args, wl, density):
             torch.cuda.synchronize()
             return ranks.max(time.perf_counter() - t0)
 
-        pinned = [batches[0][w].cpu().pin_memory() for w in range(W)]
-        dt = timed_host_steps(pinned)
+        # W x N bf16 of page-locked host memory per rank; every rank takes the
+        # same branch (the collectives inside the timing must match)
+        why = ""
+        try:
+            pinned = [batches[0][w].cpu().pin_memory() for w in range(W)]
+        except RuntimeError as ex:
+            pinned, why = None, str(ex).splitlines()[0][:160]
+        if ranks.max(0.0 if pinned is not None else 1.0) > 0.0:
+            e2e = {"unavailable": "page-locked host gradients could not be allocated on every "
+                                  f"rank ({why or 'another rank'})",
+                   "h2d_bytes_per_step": W * N * 2}
+        else:
+            dt = timed_host_steps(pinned)
+            e2e = {"value": world * N * e2e_steps / dt, "unit": "params/s",
+                   "h2d_bytes_per_step": W * N * 2,
+                   "d2h_bytes_per_step": sc.info["mask_words"] * 4,
+                   "ms_per_step": dt / e2e_steps * 1e3, "steps": e2e_steps,
+                   "host_buffers": "pinned, read in place by the step kernel",
+                   "result_read": "scape_mask_async on a side stream, overlapping the next step"}
         del pinned
-        e2e = {"value": world * N * e2e_steps / dt, "unit": "params/s",
-               "h2d_bytes_per_step": W * N * 2, "d2h_bytes_per_step": sc.info["mask_words"] * 4,
-               "ms_per_step": dt / e2e_steps * 1e3, "steps": e2e_steps,
-               "host_buffers": "pinned, read in place by the step kernel",
-               "result_read": "scape_mask_async on a side stream, overlapping the next step"}
-        if args.e2e_pageable:
+        if args.e2e_pageable and "value" in e2e:
             pageable = [batches[0][w].cpu() for w in range(W)]
             dtp = timed_host_steps(pageable)
             e2e["pageable_staged_ms_per_step"] = dtp / e2e_steps * 1e3
