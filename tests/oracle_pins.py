@@ -13,7 +13,9 @@ summary §2 and §3), stated in the oracle header:
     momentum run on the mean gradient (checked in fp64);
   - error feedback: a = b + e, and what is sent plus what is left equals
     what was accumulated;
-  - delayed mask usage: the mask applied at step t is the one built at t-1;
+  - delayed mask usage: the mask applied at step t is the one built at t-1,
+    and step 0, which has no earlier mask, applies the selection of its own
+    accumulators (recomputed here from loaded nonzero state);
   - partitioned top-k: every chunk keeps exactly floor(density*len) entries,
     the largest |a| of its owner, ties to the lower index (checked by its
     characterisation and against numpy's sort);
@@ -173,6 +175,40 @@ def pin_delayed_mask(lib: str = SO) -> None:
         assert np.array_equal(idx, o.index[used.astype(bool)])
         assert np.all(np.diff(idx.astype(np.int64)) > 0)
         prev = o.mask(0)
+
+
+# ------------------------------------------------------------ step-0 mask
+
+def pin_bootstrap_mask(lib: str = SO) -> None:
+    """Step 0 has no earlier mask, so the mask it applies (M_{-1}) is the
+    selection run on the step-0 accumulators a_w = e_w + (b1*u_w + (1-b1)*g_w)
+    before anything is written.  The state is loaded with nonzero u_w and e_w
+    first, so every term of a_w matters; a_w is recomputed here in numpy fp32
+    (one rounding per operation, as the rule states), and each chunk of the
+    applied mask must equal numpy's lexsort top-k_c of the owner's a_w, or,
+    in the non-partitioned variant, the union of every worker's top-k_c."""
+    for union in (False, True):
+        for kind in (synth.SYN_GAUSS, synth.SYN_STUDENT_Q):
+            wl = synth.tiny(5 * 1024 + 352, 3, 1024, 0.1, kind=kind, seed=14, sigma=2e-3)
+            o = oracle.Oracle.for_workload(wl, 0.1, lib_path=lib, union_mask=union)
+            rng = np.random.default_rng(40 + kind)
+            u0 = (rng.standard_normal((wl.W, o.n)) * 3e-3).astype(np.float32)
+            e0 = (rng.standard_normal((wl.W, o.n)) * 2e-3).astype(np.float32)
+            for w in range(wl.W):
+                o.set(oracle.U, u0[w], w)
+                o.set(oracle.E, e0[w], w)
+            g = np.stack([synth.cpu().grads(wl, w, 0, idx=o.index) for w in range(wl.W)])
+            o.step(g)
+            b1 = np.float32(wl.beta1)
+            c1 = np.float32(1.0) - b1
+            a0 = e0 + ((b1 * u0) + (c1 * _f32_from_bf16(g)))
+            used = o.mask(1).astype(bool)
+            for j in range(o.chunk_start.size):
+                s, ln = int(o.chunk_start[j]), int(o.chunk_len[j])
+                k = math.floor(0.1 * ln)
+                rows = a0[:, s:s + ln] if union else a0[int(o.chunk_owner[j])][None, s:s + ln]
+                ref = _union_ref(rows, k)
+                assert np.array_equal(used[s:s + ln], ref), (union, kind, j)
 
 
 # --------------------------------------------------------------- selection
@@ -423,6 +459,7 @@ def pin_union_single_worker(lib: str = SO) -> None:
 ALL_PINS = [
     pin_dense_adams, pin_single_worker_identity, pin_momentum_closed_form, pin_fixed_sum_order,
     pin_accumulator_split, pin_error_feedback_conservation, pin_delayed_mask,
+    pin_bootstrap_mask,
     pin_partitioned_topk, pin_topk_against_sort, pin_shard_geometry, pin_per_tensor_chunks,
     pin_offmask_decay,
     pin_dense_adams_single_worker, pin_dense_adams_matches_scape_density1,

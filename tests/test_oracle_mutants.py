@@ -35,6 +35,10 @@ MUTANTS = [
     ("k rounded up", "ch.k = (uint32_t)std::floor(density * (double)ch.len);",
      "ch.k = (uint32_t)std::ceil(density * (double)ch.len);"),
     ("mask not delayed", "if (o.t == 0) {", "if (true) {"),
+    ("step-0 mask from zero accumulators (first k of every chunk)", "a0[x] = o.e[x] + un;",
+     "a0[x] = 0.0f;"),
+    ("step-0 mask drops e + b1*u", "a0[x] = o.e[x] + un;", "a0[x] = c1 * g;"),
+    ("step-0 mask drops the residual", "a0[x] = o.e[x] + un;", "a0[x] = un;"),
     ("bias correction added", "float q = bb / (std::sqrt(o.v[i]) + o.eps);",
      "float q = (bb / (1.0f - std::pow(o.b1, (float)(o.t + 1)))) / (std::sqrt(o.v[i]) + o.eps);"),
     ("per-tensor chunks ignore tensor boundaries", "  if (per_tensor) {", "  if (false) {"),
