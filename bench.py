@@ -58,6 +58,8 @@ def parse():
                     help="keep the residuals in page-locked host memory")
     ap.add_argument("--union-mask", action="store_true",
                     help="the non-partitioned variant: the union of every worker's top-k")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the sweep over every layout and density (the 'workloads' rows)")
     return ap.parse_args()
 
 
@@ -116,18 +118,65 @@ def needs_l2_flush(working_bytes: int, l2_bytes: int) -> bool:
     return working_bytes < 4 * l2_bytes
 
 
-def baseline_sample_size(N: int, chunk: int, calib_rate: float, target_s: float):
-    """(chunks, steps) of the CPU-baseline sample: about target_s seconds of
-    oracle time at calib_rate coordinate-steps per second; 14 steps over as
-    many whole chunks as that allows, or every chunk over more steps when the
-    whole layout fits."""
+# The GB300's L2; the flush decision and the config's L2 note use this
+# figure on both arms (the GPU arm sizes its flush buffer from the device).
+GB300_L2_BYTES = 126 << 20
+
+# Work of the oracle sample both CPU legs time, in coordinate x worker x step
+# units: about 12 s on one Grace core (the oracle runs at about 13 M
+# coordinate-steps/s at W = 4 and its cost grows with W).
+CPU_SAMPLE_WORK = 6.4e8
+
+
+def baseline_sample_size(N: int, chunk: int, W: int, work: float = CPU_SAMPLE_WORK):
+    """(chunks, timed steps) of the oracle sample: 13 timed steps (after the
+    untimed step 0) over as many whole chunks as `work` allows, or every chunk
+    over more steps when the whole layout fits.  Fixed by the workload alone,
+    so the cpu_baseline leg and the reference arm time the same sample."""
     nch = -(-N // chunk)
-    work = calib_rate * target_s
-    n_st = 14
-    n_ch = int(work / (n_st * chunk))
+    n_st = 13
+    n_ch = int(work / (n_st * chunk * W))
     if n_ch >= nch:
-        n_ch, n_st = nch, max(14, int(work / N))
+        n_ch, n_st = nch, max(13, int(work / (N * W)))
     return max(1, n_ch), n_st
+
+
+def static_K(wl, density: float, per_tensor: bool = False) -> int:
+    """Kept coordinates per step of the partitioned rule: the sum over chunks
+    of floor(density * chunk length) (flat chunks, or each tensor's own)."""
+    import math
+    lens = []
+    if per_tensor:
+        for n in wl.numel:
+            lens += [min(wl.chunk, n - x) for x in range(0, n, wl.chunk)]
+    else:
+        nch = -(-wl.N // wl.chunk)
+        lens = [wl.chunk] * (nch - 1) + [wl.N - (nch - 1) * wl.chunk]
+    return sum(math.floor(density * ln) for ln in lens)
+
+
+def working_set_bytes(N: int, W: int, K: int, n_batches: int = 2) -> int:
+    """Bytes a step touches on the device: theta, v, u_w, e_w, the two masks,
+    the compact buffers and the gradient batches the steps alternate."""
+    return N * (8 + 8 * W) + N // 4 + K * (4 * W + 8) + n_batches * W * N * 2
+
+
+def line_config(wl, density: float, args, world: int) -> dict:
+    """The JSON line's `config`, computed from the workload alone (the same on
+    the scape and the reference arms)."""
+    K = static_K(wl, density, args.per_tensor)
+    working = working_set_bytes(wl.N, wl.W, K)
+    flush = needs_l2_flush(working, GB300_L2_BYTES)
+    return {"workload": wl.name, "N": wl.N, "W": wl.W, "density": density, "chunk": wl.chunk,
+            "seed": wl.seed, "K": K, "grad_dtype": "bf16", "grad_batches": 2,
+            "chunking": "per-tensor" if args.per_tensor else "flat",
+            "residuals": "host (page-locked)" if args.residual_host else "HBM",
+            "mask": ("union of every worker's top-k (non-partitioned)" if args.union_mask
+                     else "partitioned (SCAPE)"),
+            "parallelism": "replicas" if world > 1 else "single GPU, W emulated workers",
+            "l2": (f"flushed before every timed step (twice the L2 written, untimed): "
+                   f"{working / 1e6:.0f} MB working set" if flush else
+                   f"no flush: {working / 1e9:.1f} GB working set, far larger than the L2")}
 
 
 def alg_bytes(N: int, W: int, K: int) -> dict:
@@ -214,45 +263,190 @@ def ncu_traffic(kernel: str, N: int):
     return None, None
 
 
-def oracle_sample(wl, density, n_chunks: int, steps: int, n_batches: int = 2,
+def timed_steps(step_fn, steps: int, stream, scratch=None) -> float:
+    """Device milliseconds of `steps` calls of step_fn(i) on `stream`, from CUDA
+    events.  With `scratch` (a buffer larger than L2) the L2 is flushed before
+    every step by an untimed write and each step is timed on its own."""
+    import torch
+    if scratch is None:
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for i in range(steps):
+            step_fn(i)
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b)
+    evs = []
+    for i in range(steps):
+        scratch.fill_(i & 0xFF)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        step_fn(i)
+        b.record(stream)
+        evs.append((a, b))
+    torch.cuda.synchronize()
+    return sum(a.elapsed_time(b) for a, b in evs)
+
+
+# Every layout and density the throughput is reported on (the five workloads,
+# both densities of the 2^26 and Llama-500M layouts).
+SWEEP = [("flat-2^20-w4", 0.10), ("flat-2^26-w8-ties", 0.10), ("flat-2^26-w8-ties", 0.01),
+         ("gpt2-medium-w8", 0.01), ("llama-500m-w8", 0.01), ("llama-500m-w8", 0.10),
+         ("llama-1.8b-w4", 0.01)]
+
+
+def sweep_steps(steps: int, probe_ms: float, min_ms: float = 400.0, cap: int = 5000) -> int:
+    """Timed steps of a sweep row: at least `steps`, and enough for the timed
+    region to last min_ms (so the 100 ms clock sampler sees it under load)."""
+    want = int(np.ceil(min_ms / max(probe_ms, 1e-3)))
+    return int(min(cap, max(steps, want)))
+
+
+def time_workload(wl, density: float, steps: int, warmup: int, dev, local: int, ranks,
+                  peak: float) -> dict:
+    """One sweep row: libscape on the workload's layout, `warmup` untimed steps
+    (step 0 first), then the timed steps; L2 flushed before every timed step
+    when the working set is under four L2 sizes.  The handle and its
+    gradients are freed before returning."""
+    import torch
+    from sparse_communication_distributed_gb300 import THETA, Scape
+    world = ranks.dist.get_world_size() if ranks.dist else 1
+    N, W = wl.N, wl.W
+    sc = Scape.for_workload(wl, density)
+    try:
+        th = torch.empty(N, dtype=torch.float32, device=dev)
+        synth.gpu().theta_into(wl, th)
+        torch.cuda.synchronize()
+        sc.load(THETA, th)
+        del th
+        batches = []
+        for b in range(2):
+            bufs = [torch.empty(N, dtype=torch.int16, device=dev) for _ in range(W)]
+            for w in range(W):
+                synth.gpu().grads_into(wl, w, b, bufs[w])
+            batches.append(bufs)
+        stream = torch.cuda.current_stream(dev)
+        for i in range(warmup):
+            sc.step(batches[i % 2], stream)
+        torch.cuda.synchronize()
+        l2_bytes = torch.cuda.get_device_properties(dev).L2_cache_size
+        working = working_set_bytes(N, W, sc.K)
+        flush = needs_l2_flush(working, GB300_L2_BYTES)
+        scratch = torch.empty(2 * l2_bytes, dtype=torch.uint8, device=dev) if flush else None
+
+        def step_fn(i):
+            sc.step(batches[i % 2], stream)
+
+        probe_ms = timed_steps(step_fn, 3, stream, scratch) / 3
+        n = int(ranks.max(float(sweep_steps(steps, probe_ms))))  # the same count on every rank
+
+        def measure():
+            clocks = ClockSampler(local)
+            clocks.start()
+            time.sleep(0.3)
+            ranks.barrier()
+            torch.cuda.synchronize()
+            ms = timed_steps(step_fn, n, stream, scratch)
+            ranks.barrier()
+            return ms, clocks.stop()
+
+        ms, clk = measure()
+        if clk and THROTTLED & set(clk["reasons"]):
+            first = sorted(THROTTLED & set(clk["reasons"]))
+            ms, clk = measure()
+            if clk:
+                clk["remeasured_after"] = first
+        ms_per_step = ranks.max(ms) / n
+        info = sc._info()
+        K = sc.K
+        ab = alg_bytes(N, W, K)["step"]
+        gbs = ab / (ms_per_step * 1e-3) / 1e9
+        row = {"workload": wl.name, "density": density, "N": N, "W": W, "chunk": wl.chunk,
+               "K": K, "steps": n, "ms_per_step": ms_per_step,
+               "params_per_s": world * N / (ms_per_step * 1e-3),
+               "alg_bytes_per_step": ab, "achieved_gbs": gbs, "frac": gbs / peak,
+               "frac_of_8tbs": gbs / NOMINAL_HBM_GBS,
+               "select_fallback_chunks": info["select_fallbacks"],
+               "steps_run": info["step"],
+               "l2": (f"flushed before every timed step ({2 * l2_bytes >> 20} MB written, "
+                      f"untimed): {working / 1e6:.0f} MB working set" if flush else
+                      f"no flush: {working / 1e9:.1f} GB working set"),
+               "clocks": clk}
+        del batches, scratch
+        return row
+    finally:
+        sc.close()
+        torch.cuda.empty_cache()
+
+
+def link_copy_gbs(dev, nbytes=1 << 30, reps=3):
+    """Copy-engine rates of the host link from page-locked memory, each
+    direction alone: (host-to-device GB/s, device-to-host GB/s), best of
+    `reps` 1 GiB copies timed with CUDA events."""
+    import torch
+    h = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    d = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    s = torch.cuda.Stream(dev)
+    best = [0.0, 0.0]
+    for _ in range(reps):
+        for j, (dst, src) in enumerate(((d, h), (h, d))):
+            torch.cuda.synchronize(dev)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(s)
+            with torch.cuda.stream(s):
+                dst.copy_(src, non_blocking=True)
+            b.record(s)
+            torch.cuda.synchronize(dev)
+            best[j] = max(best[j], nbytes / (a.elapsed_time(b) * 1e-3) / 1e9)
+    del h, d
+    return best[0], best[1]
+
+
+def oracle_sample(wl, density, n_chunks: int, steps: int, warm: int = 1, n_batches: int = 2,
                   union_mask: bool = False):
     """Time the oracle (as it stands) on n_chunks whole chunks spread over the
-    shards, for ``steps`` steps over ``n_batches`` gradient batches used in
-    turn (generated before the timed loop).  Returns (params/s, seconds,
-    sample params, chunks)."""
+    shards: `warm` untimed steps (step 0 first), then `steps` timed steps,
+    over ``n_batches`` gradient batches used in turn (generated before the
+    loop).  Returns (params/s, timed seconds, sample params, chunks)."""
     import oracle
     nch = -(-wl.N // wl.chunk)
     ids = np.unique(np.linspace(0, nch - 1, n_chunks).astype(np.int64))
     o = oracle.Oracle.for_workload(wl, density, chunk_ids=ids, union_mask=union_mask)
     o.set(oracle.THETA, synth.cpu().theta0(wl, o.index))
     grads = [np.stack([synth.cpu().grads(wl, w, t, idx=o.index) for w in range(wl.W)])
-             for t in range(min(n_batches, steps))]
+             for t in range(min(n_batches, warm + steps))]
+    for t in range(warm):
+        o.step(grads[t % len(grads)])
     t0 = time.perf_counter()
-    for t in range(steps):
+    for t in range(warm, warm + steps):
         o.step(grads[t % len(grads)])
     dt = time.perf_counter() - t0
     return o.n * steps / dt, dt, o.n, ids.size
+
+
+def cpu_sample_note(wl, density, nc, n, warm, steps, dt) -> str:
+    return (f"{nc} whole chunks ({n} params) of {wl.name}, W={wl.W}, density {density}: "
+            f"{warm} untimed step(s) (step 0 first), then {steps} timed steps over 2 gradient "
+            f"batches, {dt:.1f} s of oracle time; single-threaded C++ oracle on one host core")
 
 
 def run_reference(args, wl, density):
     rank, world, _ = dist_env()
     if rank != 0:
         return
-    n_chunks = 16 if wl.N > 1 << 24 else max(1, min(16, -(-wl.N // wl.chunk)))
-    steps = args.warmup + args.steps
-    rate, dt, n, nc = oracle_sample(wl, density, n_chunks, steps, union_mask=args.union_mask)
-    per_step_ms = dt / steps * 1e3
-    sample = (f"{nc} whole chunks ({n} params) of {wl.name}, W={wl.W}, density {density}, "
-              f"{steps} steps incl. step 0; single-threaded C++ oracle")
+    n_chunks, _ = baseline_sample_size(wl.N, wl.chunk, wl.W)
+    rate, dt, n, nc = oracle_sample(wl, density, n_chunks, args.steps, warm=args.warmup,
+                                    union_mask=args.union_mask)
+    per_step_ms = dt / args.steps * 1e3
     line = {
         "impl": "reference", "metric": METRIC, "value": rate, "unit": "params/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": per_step_ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": wl.name, "N": wl.N, "W": wl.W, "density": density,
-                   "chunk": wl.chunk, "seed": wl.seed, "sample_params": n},
+        "config": line_config(wl, density, args, world),
         "cpu_baseline": {"value": rate, "unit": "params/s", "cores": 1, "kind": "oracle",
-                         "sample": sample},
+                         "sample": cpu_sample_note(wl, density, nc, n, args.warmup, args.steps,
+                                                   dt)},
         "e2e": {"value": rate, "unit": "params/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -332,30 +526,12 @@ def run_scape(args, wl, density):
     # A working set that L2 could hold is evicted before every timed step by
     # writing a buffer of twice the L2 size (untimed); larger ones are not.
     l2_bytes = torch.cuda.get_device_properties(dev).L2_cache_size
-    working = sc.info["device_bytes"] + W * N * 2 * n_batches
-    flush = needs_l2_flush(working, l2_bytes)
+    config = line_config(wl, density, args, world)
+    flush = needs_l2_flush(working_set_bytes(N, W, config["K"], n_batches), GB300_L2_BYTES)
     scratch = torch.empty(2 * l2_bytes, dtype=torch.uint8, device=dev) if flush else None
 
     def timed(step_fn, steps):
-        """Device milliseconds of `steps` calls of step_fn(i) on `stream`."""
-        if not flush:
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            for i in range(steps):
-                step_fn(i)
-            b.record(stream)
-            torch.cuda.synchronize()
-            return a.elapsed_time(b)
-        evs = []
-        for i in range(steps):
-            scratch.fill_(i & 0xFF)
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            step_fn(i)
-            b.record(stream)
-            evs.append((a, b))
-        torch.cuda.synchronize()
-        return sum(a.elapsed_time(b) for a, b in evs)
+        return timed_steps(step_fn, steps, stream, scratch)
 
     def measure():
         clocks = ClockSampler(local)
@@ -424,12 +600,21 @@ def run_scape(args, wl, density):
                    "h2d_bytes_per_step": W * N * 2}
         else:
             dt = timed_host_steps(pinned)
+            h2d_bytes = W * N * 2
+            link_h2d, link_d2h = link_copy_gbs(dev)
+            got_h2d = h2d_bytes / (dt / e2e_steps) / 1e9
             e2e = {"value": world * N * e2e_steps / dt, "unit": "params/s",
-                   "h2d_bytes_per_step": W * N * 2,
+                   "h2d_bytes_per_step": h2d_bytes,
                    "d2h_bytes_per_step": sc.info["mask_words"] * 4,
                    "ms_per_step": dt / e2e_steps * 1e3, "steps": e2e_steps,
                    "host_buffers": "pinned, read in place by the step kernel",
-                   "result_read": "scape_mask_async on a side stream, overlapping the next step"}
+                   "result_read": "scape_mask_async on a side stream, overlapping the next step",
+                   "link_h2d_gbs": link_h2d, "link_d2h_gbs": link_d2h,
+                   "achieved_h2d_gbs": got_h2d, "frac_of_link": got_h2d / link_h2d,
+                   "link_bound_ms": h2d_bytes / (link_h2d * 1e9) * 1e3,
+                   "link_note": "link_*: copy-engine rate of 1 GiB page-locked copies in each "
+                                "direction alone, measured in this run; the step reads its "
+                                "gradients over the link while M_t goes back on a side stream"}
         del pinned
         if args.e2e_pageable and "value" in e2e:
             pageable = [batches[0][w].cpu() for w in range(W)]
@@ -475,16 +660,11 @@ def run_scape(args, wl, density):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        # sized from a short calibration run, which includes step 0 and so
-        # reads slow: a 15 s target lands near 12 s of oracle time
-        nch = -(-N // wl.chunk)
-        r0, _, _, _ = oracle_sample(wl, density, min(8, nch), 3, union_mask=args.union_mask)
-        n_ch, n_st = baseline_sample_size(N, wl.chunk, r0, 15.0)
-        rate, dt, n, nc = oracle_sample(wl, density, n_ch, n_st, union_mask=args.union_mask)
+        n_ch, n_st = baseline_sample_size(N, wl.chunk, W)
+        rate, dt, n, nc = oracle_sample(wl, density, n_ch, n_st, warm=1,
+                                        union_mask=args.union_mask)
         cpu = {"value": rate, "unit": "params/s", "cores": 1, "kind": "oracle",
-               "sample": f"{nc} whole chunks ({n} params) of {wl.name}, W={W}, density {density}, "
-                         f"{n_st} steps incl. step 0 over 2 gradient batches, {dt:.1f} s of "
-                         f"oracle time; single-threaded C++ oracle on one host core"}
+               "sample": cpu_sample_note(wl, density, nc, n, 1, n_st, dt)}
 
     link = None
     if args.residual_host:
@@ -495,10 +675,37 @@ def run_scape(args, wl, density):
                 "duplex_copy_gbs": duplex,
                 "frac": rb / (ms_per_step * 1e-3) / 1e9 / duplex,
                 "peak_kind": "measured here: concurrent page-locked copies in both directions"}
+    peak, peak_kind = measured_peak()
+    fallbacks = sc._info()["select_fallbacks"]
+    workloads = None
+    variant = (args.per_tensor or args.residual_host or args.union_mask or args.workers is not None
+               or args.seed is not None or args.density is not None)
+    if not args.no_workloads and not variant and wl.name == synth.BENCH_WORKLOAD:
+        # every layout and density, one handle at a time (the headline row is
+        # the measurement above)
+        sc.close()
+        del batches
+        torch.cuda.empty_cache()
+        workloads = []
+        for name, d in SWEEP:
+            if name == wl.name and d == density:
+                gbs = alg_bytes(N, W, K)["step"] / (ms_per_step * 1e-3) / 1e9
+                workloads.append({"workload": name, "density": d, "N": N, "W": W,
+                                  "chunk": wl.chunk, "K": K, "steps": args.steps,
+                                  "ms_per_step": ms_per_step,
+                                  "params_per_s": world * N / (ms_per_step * 1e-3),
+                                  "alg_bytes_per_step": alg_bytes(N, W, K)["step"],
+                                  "achieved_gbs": gbs, "frac": gbs / peak,
+                                  "frac_of_8tbs": gbs / NOMINAL_HBM_GBS,
+                                  "select_fallback_chunks": fallbacks,
+                                  "l2": "no flush (the line's own measurement)", "clocks": clk,
+                                  "headline": True})
+                continue
+            workloads.append(time_workload(synth.WORKLOADS[name], d, args.steps, args.warmup,
+                                           dev, local, ranks, peak))
     if rank != 0:
         ranks.close()
         return
-    peak, peak_kind = measured_peak()
     ab = alg_bytes(N, W, K)
     traffic, traffic_src = ncu_traffic("step_chunks", N)
     if args.union_mask:  # the counters were captured on the partitioned kernel
@@ -520,18 +727,7 @@ def run_scape(args, wl, density):
         "vs_baseline": None,
         "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": wl.name, "N": N, "W": W, "density": density, "chunk": wl.chunk,
-                   "seed": wl.seed,
-                   "K": K, "grad_dtype": "bf16", "grad_batches": n_batches,
-                   "chunking": "per-tensor" if args.per_tensor else "flat",
-                   "residuals": "host (page-locked)" if args.residual_host else "HBM",
-                   "mask": ("union of every worker's top-k (non-partitioned)" if args.union_mask
-                            else "partitioned (SCAPE)"),
-                   "parallelism": "replicas" if world > 1 else "single GPU, W emulated workers",
-                   "l2": (f"flushed before every timed step ({2 * l2_bytes >> 20} MB written, "
-                          f"untimed): {working / 1e6:.0f} MB working set" if flush else
-                          f"no flush: {working / 1e9:.1f} GB working set, far larger than "
-                          f"the {l2_bytes >> 20} MB L2")},
+        "config": config,
         "step_hbm": {"alg_bytes_per_step": ab["step"], "achieved_gbs": step_gbs,
                      "frac_of_8tbs": step_gbs / NOMINAL_HBM_GBS,
                      "frac_of_peak": step_gbs / peak, "peak_kind": peak_kind},
@@ -543,14 +739,17 @@ def run_scape(args, wl, density):
         "kernels_ms_per_step": {k: v[0] / args.steps for k, v in phases.items() if v[1]},
         "gpu_launches": args.steps * 2,
         "step0_ms": step0_ms,
-        "select_fallback_chunks": sc._info()["select_fallbacks"],
+        "select_fallback_chunks": fallbacks,
         "clocks": clk,
         "e2e": e2e,
         "residual_link": link,
         "dense_adams": dense,
         "mask_stats": mstats,
         "cpu_baseline": cpu,
+        "workloads": workloads,
     }
+    if args.union_mask:
+        line["union_K"] = K  # compact values per worker in the last step (the union's fill-in)
     print(json.dumps(line), flush=True)
     ranks.close()
 

@@ -310,20 +310,25 @@ int scape_dense_adams_step(float* theta, float* m, float* v, const void* const* 
  * step-0 mask into mask_prev, as scape_step does on a new handle.  Between
  * calls the caller swaps mask_prev and mask_next.
  *
+ * Every buffer and gradient pointer must be device (or managed) memory of
+ * the current device; a host, freed or foreign pointer -> SCAPE_EINVAL
+ * (checked with cudaPointerGetAttributes before anything is enqueued).
+ *
  * Scratch: the step needs one flag per chunk and a counter.  They live in a
  * static device array inside the library, sized for at most 65536 chunks
  * (256 KiB), which every GPU that loads the library holds until the process
- * exits.  More chunks -> SCAPE_EINVAL.  Each call clears the part it uses
- * with cudaMemsetAsync on "stream" (the array keeps the last call's
- * contents otherwise).  All calls share the one array, so calls whose work
- * overlaps on the GPU (different streams without ordering, or several
- * threads) race on it: order them on one stream.
+ * exits.  More chunks -> SCAPE_EINVAL.  The array keeps the last call's
+ * contents: a call that completes leaves every flag clear again (the
+ * standalone select clears each flag it handles).  All calls share the one
+ * array, so calls whose work overlaps on the GPU (different streams without
+ * ordering, or several threads) race on it: order them on one stream.
  *
  * The first call on each device looks up the array's device address
- * (cudaGetSymbolAddress) and sets the kernel's shared-memory limit; make
- * that first call before any stream capture.  No call allocates device or
- * pinned memory, and nothing calls cudaMalloc, cudaFree or an allocating
- * library routine.
+ * (cudaGetSymbolAddress), clears the whole array (cudaMemsetAsync on
+ * "stream", then cudaStreamSynchronize) and sets the kernel's shared-memory
+ * limit; make that first call before any stream capture.  No call allocates
+ * device or pinned memory, and nothing calls cudaMalloc, cudaFree or an
+ * allocating library routine.
  *
  * Returns SCAPE_OK or SCAPE_EINVAL / SCAPE_ECUDA; the message is available
  * from scape_last_error(NULL) on the calling thread.  The work is enqueued on

@@ -43,6 +43,25 @@ int fail(int code, const char* fmt, ...) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Device (or managed) memory of the current device "dev".  A host pointer, a
+// freed pointer or another device's memory would fault the kernels, so it is
+// rejected here; the query allocates nothing.  Without a usable CUDA device
+// the query itself fails, which is reported the same way.
+int check_device_ptr(const void* p, int dev, const char* what) {
+  cudaPointerAttributes at;
+  cudaError_t e = cudaPointerGetAttributes(&at, p);
+  if (e != cudaSuccess) {
+    cudaGetLastError();  // the query's error is not sticky; do not leave it behind
+    return fail(SCAPE_EINVAL, "%s is not a device pointer (%s)", what, cudaGetErrorString(e));
+  }
+  const bool ok = at.type == cudaMemoryTypeManaged ||
+                  (at.type == cudaMemoryTypeDevice && at.device == dev);
+  if (!ok)
+    return fail(SCAPE_EINVAL, "%s must be device memory of the current device %d "
+                "(memory type %d, device %d)", what, dev, (int)at.type, at.device);
+  return SCAPE_OK;
+}
+
 }  // namespace
 
 SCAPE_API int scape_step_noalloc(const scape_step_buffers* b, const void* const* grad_ptrs,
@@ -88,11 +107,27 @@ SCAPE_API int scape_step_noalloc(const scape_step_buffers* b, const void* const*
     if (!grad_ptrs[w] || !aligned16(grad_ptrs[w]))
       return fail(SCAPE_EINVAL, "grad_ptrs[%d] must be a 16-byte aligned device pointer", w);
 
-  // first call on this device: the device address of the scratch array
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return fail(SCAPE_ECUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  // every buffer must be memory of the current device (checked before any launch)
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    dev = -1;
+  }
+  static const char* const names[] = {"theta", "v", "u", "e", "mask_prev", "mask_next", "vals",
+                                      "bbar", "idx"};
+  for (int j = 0; j < 9; j++)
+    if (int rc = check_device_ptr(ptrs[j], dev, names[j])) return rc;
+  for (int w = 0; w < W; w++) {
+    char what[32];
+    snprintf(what, sizeof what, "grad_ptrs[%d]", w);
+    if (int rc = check_device_ptr(grad_ptrs[w], dev, what)) return rc;
+  }
+
+  // first call on this device: the device address of the scratch array, and
+  // one clear of the whole array (it stays clear: see below)
   if (dev < 0 || dev >= kMaxDevices) return fail(SCAPE_EINVAL, "device %d not supported", dev);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
   uint32_t* scratch;
   {
     std::lock_guard<std::mutex> lock(g_mu);
@@ -101,17 +136,22 @@ SCAPE_API int scape_step_noalloc(const scape_step_buffers* b, const void* const*
       e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
       if (e != cudaSuccess || !p)
         return fail(SCAPE_ECUDA, "cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+      if ((e = cudaMemsetAsync(p, 0, sizeof(g_noalloc_scratch), s)) != cudaSuccess ||
+          (e = cudaStreamSynchronize(s)) != cudaSuccess)
+        return fail(SCAPE_ECUDA, "clearing the scratch: %s", cudaGetErrorString(e));
       g_scratch_ptr[dev] = static_cast<uint32_t*>(p);
     }
     scratch = g_scratch_ptr[dev];
   }
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // the flags and the counter must start at zero; the array keeps the last call's contents
-  if ((e = cudaMemsetAsync(scratch, 0, (n_ch + 1) * sizeof(uint32_t), s)) != cudaSuccess)
-    return fail(SCAPE_ECUDA, "clearing the scratch: %s", cudaGetErrorString(e));
-  // scratch layout within the array: flags at [0, n_ch), counter at [n_ch]
+  // scratch layout within the array: flags at [0, n_ch), counter at [kMaxChunks].
+  // The step kernel sets the flag of a chunk it leaves to the standalone
+  // select, and the select clears every flag it handles, so a call that
+  // completes leaves the flags clear for the next.  (A call that failed
+  // between its launches may leave flags set; the next call then redoes
+  // those chunks' selection from the same state, which gives the same mask.)
+  // The counter only counts flagged chunks and is never read here.
   uint32_t* flags = scratch;
-  uint32_t* counter = scratch + n_ch;
+  uint32_t* counter = scratch + kMaxChunks;
 
   SelectArgs sa{};
   for (int w = 0; w < W; w++) sa.grads[w] = static_cast<const uint16_t*>(grad_ptrs[w]);

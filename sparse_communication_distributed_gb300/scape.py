@@ -265,6 +265,8 @@ def step_noalloc(numel, chunk: int, W: int, density: float, hyper, buffers: dict
     (beta1, beta2, lr, wd, eps); ``buffers`` maps theta, v, u, e, mask_prev,
     mask_next, vals, bbar, idx to tensors and row_stride, vals_stride to ints."""
     lib = load_library()
+    if len(grads) != W:
+        raise ValueError(f"step_noalloc: {len(grads)} gradient buffers for W={W}")
     arr = np.ascontiguousarray(numel, dtype=np.uint64)
     lay = _Layout(arr.size, arr.ctypes.data_as(ctypes.POINTER(ctypes.c_uint64)), chunk)
     b1, b2, lr, wd, eps = hyper

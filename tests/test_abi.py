@@ -143,3 +143,22 @@ def test_dense_rejects_bad_hyper_parameters(lib, hyper):
     assert rc == scape.SCAPE_EINVAL
     assert "hyper-parameters" in lib.scape_last_error(None).decode()
 
+
+
+def test_noalloc_rejects_host_buffers(lib):
+    # host memory in every buffer (aligned, non-null): rejected as not device
+    # memory before anything is enqueued; without a GPU the pointer query
+    # itself fails, which is reported the same way
+    N, W = 1024, 2
+    raw = np.zeros(N * 16 + 16, np.float32)
+    off = (-raw.ctypes.data % 16) // 4
+    host = raw[off:off + N * 16]
+    p = host.ctypes.data
+    arr = np.asarray([N], np.uint64)
+    lay = scape._Layout(1, arr.ctypes.data_as(ctypes.POINTER(ctypes.c_uint64)), 1024)
+    sb = scape.StepBuffers(ctypes.pointer(lay), W, 0.1, 0.9, 0.95, 1e-3, 0.1, 1e-8,
+                           p, p + 4096, p + 8192, p + 16384, N, p + 24576, p + 28672,
+                           p + 32768, N, p + 40960, p + 45056, 1)
+    grads = (ctypes.c_void_p * W)(p + 49152, p + 53248)
+    assert lib.scape_step_noalloc(ctypes.byref(sb), grads, None) == scape.SCAPE_EINVAL
+    assert "device" in lib.scape_last_error(None).decode()

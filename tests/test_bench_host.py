@@ -56,12 +56,45 @@ def test_l2_flush_rule():
 
 
 def test_baseline_sample_size():
-    # large layout: 14 steps over as many chunks as the time allows
-    assert bench.baseline_sample_size(1_775_372_288, 65536, 6.4e6, 15.0) == (104, 14)
+    # large layout: 13 timed steps over as many chunks as the work allows
+    assert bench.baseline_sample_size(1_775_372_288, 65536, 4) == (187, 13)
+    assert bench.baseline_sample_size(557_774_080, 65536, 8) == (93, 13)
     # small layout: every chunk, more steps
-    assert bench.baseline_sample_size(1 << 20, 4096, 7.9e6, 15.0) == (256, 113)
-    # never below 14 steps or one chunk
-    assert bench.baseline_sample_size(1 << 20, 4096, 1.0, 15.0) == (1, 14)
+    assert bench.baseline_sample_size(1 << 20, 4096, 4) == (256, 152)
+    # never below 13 steps or one chunk
+    assert bench.baseline_sample_size(1 << 20, 4096, 4, work=1.0) == (1, 13)
+
+
+@pytest.mark.parametrize("name,density,K", [
+    ("flat-2^20-w4", 0.10, 104_704), ("flat-2^26-w8-ties", 0.01, 670_720),
+    ("gpt2-medium-w8", 0.01, 3_546_282), ("llama-500m-w8", 0.10, 55_772_302),
+    ("llama-1.8b-w4", 0.01, 17_743_970)])
+def test_static_K_matches_the_tabulated_counts(name, density, K):
+    assert bench.static_K(bench.synth.WORKLOADS[name], density) == K
+
+
+def test_line_config_is_the_same_on_both_arms():
+    import types
+    args = types.SimpleNamespace(per_tensor=False, residual_host=False, union_mask=False)
+    wl = bench.synth.WORKLOADS["llama-1.8b-w4"]
+    c = bench.line_config(wl, 0.01, args, 1)
+    assert c["K"] == 17_743_970 and c["l2"].startswith("no flush")
+    assert bench.line_config(wl, 0.01, args, 1) == c
+    small = bench.line_config(bench.synth.WORKLOADS["flat-2^20-w4"], 0.1, args, 1)
+    assert small["l2"].startswith("flushed before every timed step")
+
+
+def test_sweep_rows_cover_every_config_and_density():
+    rows = {(n, d) for n, d in bench.SWEEP}
+    for name in ("flat-2^20-w4", "flat-2^26-w8-ties", "gpt2-medium-w8", "llama-500m-w8",
+                 "llama-1.8b-w4"):
+        for d in bench.synth.WORKLOADS[name].densities:
+            assert (name, d) in rows
+    assert len(rows) == 7
+    # timed steps: at least the requested count, enough for 400 ms, capped
+    assert bench.sweep_steps(20, 23.6) == 20
+    assert bench.sweep_steps(20, 1.7) == 236
+    assert bench.sweep_steps(20, 0.03) == 5000
 
 
 def test_clock_parse_and_throttle_rule():
