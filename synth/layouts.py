@@ -122,6 +122,12 @@ WORKLOADS["profile-2^25-w4"] = Workload(
     "profile-2^25-w4", (("flat", (1 << 25,)),), W=4, chunk=65536, densities=(0.01,), steps=3,
     sigma=1e-3, description="one tensor of 2^25, W=4, density 0.01, chunk 65536 (profiling case)")
 
+# Half of it: a second capture point, to show the kernel's DRAM bytes per
+# coordinate do not change with the size.
+WORKLOADS["profile-2^24-w4"] = Workload(
+    "profile-2^24-w4", (("flat", (1 << 24,)),), W=4, chunk=65536, densities=(0.01,), steps=3,
+    sigma=1e-3, description="one tensor of 2^24, W=4, density 0.01, chunk 65536 (profiling case)")
+
 # The workload the throughput line is quoted on.
 BENCH_WORKLOAD = "llama-1.8b-w4"
 
