@@ -245,22 +245,28 @@ class ClockSampler:
                 "reasons": sorted(reasons)}
 
 
-def ncu_traffic(kernel: str, N: int):
+def ncu_traffic(kernel: str, N: int, workload: str | None = None):
     """Per-launch DRAM bytes (read + write) of the kernel from the committed ncu
-    summary: bytes per coordinate measured on a smaller capture of the same
-    kernel, times N (its traffic grows in proportion to the coordinates).
-    None when the summary was taken on another source of the kernel."""
+    summary: bytes per coordinate of a one-launch capture, times N.  A capture
+    on the workload itself is preferred; otherwise one on a smaller layout of
+    the same kernel is scaled (its traffic grows in proportion to the
+    coordinates).  None when every capture was taken on another source of the
+    kernel."""
     src = {"step_chunks": "k_fused.cu"}.get(kernel)
     path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
     if not src or not os.path.exists(path):
         return None, None
     h = hashlib.sha256(open(os.path.join(ROOT, "sparse_communication_distributed_gb300", "csrc",
                                          src), "rb").read()).hexdigest()[:16]
+    found = None
     for line in open(path):
         f = line.split()
         if len(f) >= 4 and f[0] == kernel and f[3] == h:
-            return float(f[2]) * N, f"scaled from an ncu capture on {f[1]}"
-    return None, None
+            if workload is not None and f[1] == workload:
+                return float(f[2]) * N, f"ncu capture on {f[1]} itself (one launch)"
+            if found is None:
+                found = (float(f[2]) * N, f"scaled from an ncu capture on {f[1]}")
+    return found if found else (None, None)
 
 
 def timed_steps(step_fn, steps: int, stream, scratch=None) -> float:
@@ -707,7 +713,7 @@ def run_scape(args, wl, density):
         ranks.close()
         return
     ab = alg_bytes(N, W, K)
-    traffic, traffic_src = ncu_traffic("step_chunks", N)
+    traffic, traffic_src = ncu_traffic("step_chunks", N, wl.name)
     if args.union_mask:  # the counters were captured on the partitioned kernel
         traffic, traffic_src = None, None
     a_ms, a_n = phases["step"]

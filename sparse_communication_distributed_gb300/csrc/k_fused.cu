@@ -26,8 +26,9 @@
 //     every key below dropped, and the coordinates inside it (usually a few
 //     hundred) get their full 31-bit keys back from what phase 1 wrote (vals
 //     on the applied mask, else the new residual) and are ranked on the
-//     unique composite (key << 16 | 0xFFFF - index).  The chunk's mask words
-//     are assembled in shared memory and stored.  A bucket with more than
+//     unique composite (key << 16 | 0xFFFF - index); one pass over the stored
+//     keys both assembles the chunk's mask words in shared memory and lists
+//     the bucket's coordinates.  A bucket with more than
 //     kCap coordinates (massive ties) flags the chunk; the standalone radix
 //     select redoes such chunks after this kernel;
 //  3. the streaming pass of every other worker;
@@ -450,64 +451,59 @@ __device__ bool select_chunk(const FusedArgs& p, const Shared& sh, const Chunk& 
     if (!take_bucket) {
       if (cnt16 > kCap) return false;  // uniform: every thread read the same cnt16
       ranked = true;
-      // candidates: coordinates in bucket T16, with their full composite key.
-      // Lane l of a warp tests keys [b0 + 8 l, b0 + 8 l + 8) (one 16-byte
-      // load); the rare rounds with a match allocate slots by a warp scan.
-      for (uint32_t b0 = (tid & ~31u) * 8; b0 < L; b0 += K::NT * 8) {
-        const uint32_t i0 = b0 + lane * 8;
-        uint32_t m8 = 0;  // bit j: coordinate i0 + j is in the bucket
-        if (i0 + 8 <= L) {
-          const uint4 v = *reinterpret_cast<const uint4*>(sh.key16 + i0);
-          const uint32_t kw[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-          for (int q = 0; q < 8; q++)
-            m8 |= (uint32_t)(((kw[q >> 1] >> (16 * (q & 1))) & 0xFFFFu) == T16) << q;
-        } else {
-          for (uint32_t q = 0; i0 + q < L; q++) m8 |= (uint32_t)(sh.key16[i0 + q] == T16) << q;
-        }
-        if (!__any_sync(kFull, m8 != 0u)) continue;  // warp-uniform
-        const uint32_t n = __popc(m8);
-        const uint32_t incl = warp_incl_scan(n, lane);
-        uint32_t pos = 0;
-        if (lane == 31) pos = atomicAdd(&sh.ctl[C_NCAND], incl);
-        pos = __shfl_sync(kFull, pos, 31) + incl - n;
-        for (uint32_t mm = m8; mm; mm &= mm - 1u) {
-          const uint32_t i = i0 + (uint32_t)(__ffs(mm) - 1);
-          const uint32_t slot = pos++;
-          if (SCAPE_CHECK(p.dbg, slot < kCap, CHK_CAND, ch.c0 + i)) {
-            const uint32_t key = owner_key(p, sh, ch, i);
-            sh.cand[slot] = ((unsigned long long)key << 16) | (unsigned long long)(0xFFFFu - i);
-          }
-        }
-      }
-      __syncthreads();
-      ncand = sh.ctl[C_NCAND];
     }
   }
 
-  // mask words from the stored keys: lane l of a warp tests keys
-  // [b0 + 8 l, b0 + 8 l + 8) (one 16-byte load; a warp covers 8 words) into
-  // a byte, and the 4 lanes of a word merge their bytes by two xor-shuffles
+  // One pass over the stored keys builds the chunk's mask words (kept iff
+  // key16 >= tb) and, when the threshold bucket must be ranked, lists its
+  // coordinates with their full composite keys.  Lane l of a warp tests keys
+  // [b0 + 8 l, b0 + 8 l + 8) (one 16-byte load; a warp covers 8 words) into a
+  // byte, and the 4 lanes of a word merge their bytes by two xor-shuffles;
+  // the rare rounds where some lane holds a bucket key allocate list slots by
+  // a warp scan.
   const int warp = tid >> 5;
   const uint32_t tb = take_bucket ? T16 : T16 + 1;  // kept iff key16 >= tb
   for (uint32_t b0 = (uint32_t)warp * 256; b0 < ch.nw * 32; b0 += K::NT * 8) {
     const uint32_t i0 = b0 + lane * 8;
-    uint32_t byte = 0u;
+    uint32_t byte = 0u, m8 = 0u;  // m8 bit j: coordinate i0 + j is in the bucket
     if (i0 + 8 <= L) {
       const uint4 v = *reinterpret_cast<const uint4*>(sh.key16 + i0);
       const uint32_t kw[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-      for (int q = 0; q < 8; q++)
-        byte |= (uint32_t)(((kw[q >> 1] >> (16 * (q & 1))) & 0xFFFFu) >= tb) << q;
+      for (int q = 0; q < 8; q++) {
+        const uint32_t k16 = (kw[q >> 1] >> (16 * (q & 1))) & 0xFFFFu;
+        byte |= (uint32_t)(k16 >= tb) << q;
+        m8 |= (uint32_t)(k16 == T16) << q;
+      }
     } else {
-      for (uint32_t q = 0; i0 + q < L; q++) byte |= (uint32_t)(sh.key16[i0 + q] >= tb) << q;
+      for (uint32_t q = 0; i0 + q < L; q++) {
+        const uint32_t k16 = sh.key16[i0 + q];
+        byte |= (uint32_t)(k16 >= tb) << q;
+        m8 |= (uint32_t)(k16 == T16) << q;
+      }
     }
     uint32_t word = byte << (8 * (lane & 3));
     word |= __shfl_xor_sync(kFull, word, 1);
     word |= __shfl_xor_sync(kFull, word, 2);
     if ((lane & 3) == 0 && (i0 >> 5) < ch.nw) sh.mword[i0 >> 5] = word;
+    if (!ranked) continue;
+    if (!__any_sync(kFull, m8 != 0u)) continue;  // warp-uniform
+    const uint32_t n = __popc(m8);
+    const uint32_t incl = warp_incl_scan(n, lane);
+    uint32_t pos = 0;
+    if (lane == 31) pos = atomicAdd(&sh.ctl[C_NCAND], incl);
+    pos = __shfl_sync(kFull, pos, 31) + incl - n;
+    for (uint32_t mm = m8; mm; mm &= mm - 1u) {
+      const uint32_t i = i0 + (uint32_t)(__ffs(mm) - 1);
+      const uint32_t slot = pos++;
+      if (SCAPE_CHECK(p.dbg, slot < kCap, CHK_CAND, ch.c0 + i)) {
+        const uint32_t key = owner_key(p, sh, ch, i);
+        sh.cand[slot] = ((unsigned long long)key << 16) | (unsigned long long)(0xFFFFu - i);
+      }
+    }
   }
   __syncthreads();
+  if (ranked) ncand = sh.ctl[C_NCAND];
 
   if (ranked) {
     if (ncand <= kRankCountMax) {

@@ -39,10 +39,15 @@ def test_traffic_lookup_needs_the_captured_source(tmp_path, monkeypatch):
     prof.mkdir()
     import hashlib
     h = hashlib.sha256(b"kernel source A\n").hexdigest()[:16]
-    (prof / "ncu_traffic.txt").write_text(f"# header\nstep_chunks some-case 80.0 {h}\n")
+    (prof / "ncu_traffic.txt").write_text(f"# header\nstep_chunks some-case 80.0 {h}\n"
+                                          f"step_chunks the-bench 81.0 {h}\n")
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     t, where = bench.ncu_traffic("step_chunks", 1000)
     assert t == 80_000.0 and "some-case" in where
+    t, where = bench.ncu_traffic("step_chunks", 1000, "the-bench")  # a capture of the workload itself
+    assert t == 81_000.0 and "itself" in where
+    t, where = bench.ncu_traffic("step_chunks", 1000, "another")
+    assert t == 80_000.0 and "scaled" in where
     (src / "k_fused.cu").write_text("kernel source B\n")  # the kernel changed since the capture
     assert bench.ncu_traffic("step_chunks", 1000) == (None, None)
     assert bench.ncu_traffic("other_kernel", 1000) == (None, None)
