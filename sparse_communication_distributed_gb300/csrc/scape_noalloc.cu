@@ -8,8 +8,8 @@
 // file-scope array below, sized for kMaxChunks chunks, which every GPU that
 // loads the library holds until the process exits.  Host code cannot use
 // the array's name as a device address, so the first call on each device
-// looks the address up with cudaGetSymbolAddress (with that device current)
-// and keeps it.
+// looks the address up with cudaGetSymbolAddress (with that device current),
+// clears the array once and keeps the address.
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>

@@ -20,7 +20,7 @@ if not torch.cuda.is_available():
 import oracle  # noqa: E402
 import synth  # noqa: E402
 from gpu_harness import DeviceRun, OracleRun, check_full_mask, compare, sample_chunks  # noqa: E402
-from sparse_communication_distributed_gb300 import E, MASK, STEP, THETA, U, V, Scape  # noqa: E402
+from sparse_communication_distributed_gb300 import E, MASK, STEP, THETA, U, V  # noqa: E402
 
 pytestmark = pytest.mark.gpu
 

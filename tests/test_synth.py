@@ -3,7 +3,6 @@ deviates' moments, bf16 rounding, determinism, and the workload layouts."""
 import math
 
 import numpy as np
-import pytest
 
 import synth
 
